@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the partitioned-attention hot path on GB300.
+
+One benchmark step = one stream tick of the whole hot path:
+  * gamma of AdaRMSNorm for every (layer, site, denoising step) of the tick
+    (one launch: gamma depends only on t_k, the robot state and the weights),
+  * ring append of the new frame into all layers' windows,
+  * K denoising steps x L layers of {AdaRMSNorm, partitioned attention,
+    AdaRMSNorm},
+captured once as a CUDA graph and replayed.  value = denoise steps per second
+(ticks x K / time).  Inputs are seeded synthetic tensors already resident in
+HBM; two input pools larger than L2 alternate between ticks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3]
+    python bench.py --impl reference ...   # the CPU fp64 oracle, timed on host cores
+
+Under torchrun (N > 1) every rank runs an independent replica (the method has
+no cross-GPU exchange); value = all ranks' denoise steps / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from partitioned_kv_cache_gb300 import workload as W  # noqa: E402
+
+METRIC = "partitioned-attn denoise-steps/s; TFLOP/s & HBM GB/s as % of GB300 peak"
+UNIT = "denoise-steps/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def attn_flops(wl: W.Workload) -> float:
+    """Algorithmic FLOPs of one attention call (full window): 4*Hq*S*Lk*D."""
+    return 4.0 * wl.Hq * wl.S * wl.keys_full * wl.D
+
+
+def describe(wl: W.Workload) -> str:
+    return ("%s: %d layers, %d q / %d kv heads, head_dim %d, pinned %d, window %d x %d, "
+            "suffix %d, %d denoising steps per tick, AdaRMSNorm d=%d" %
+            (wl.name, wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S, wl.steps, wl.d_model))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower().startswith("active")})
+        sm = sorted(r[0] for r in rows)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU fp64 oracle (reference arm and cpu_baseline): timed as it stands
+# ---------------------------------------------------------------------------
+def oracle_sample(wl: W.Workload, seed: int, denoise_steps: int):
+    """Time the oracle over one frame push + `denoise_steps` denoising steps of
+    all layers (gamma, AdaRMSNorm, attention, AdaRMSNorm).  Returns
+    (denoise-steps/s, seconds, description)."""
+    from oracle.pipeline import OracleStream
+    st = OracleStream(wl, seed)
+    for t in range(wl.N):
+        st.push(t)
+    tick = wl.N
+    t0 = time.perf_counter()
+    st.push(tick)
+    for k in range(denoise_steps):
+        for l in range(wl.L):
+            st.norm(tick, k % wl.steps, l, 0)
+            st.attend(tick, k % wl.steps, l)
+            st.norm(tick, k % wl.steps, l, 1)
+    dt = time.perf_counter() - t0
+    return denoise_steps / dt, dt, ("1 frame push + %d denoising steps x %d layers of %s"
+                                    % (denoise_steps, wl.L, wl.name))
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    for _ in range(args.warmup):
+        oracle_sample(wl, args.seed, 1)
+    t0 = time.perf_counter()
+    steps = 0
+    for _ in range(args.steps):
+        _, _, desc = oracle_sample(wl, args.seed, 1)
+        steps += 1
+    dt = time.perf_counter() - t0
+    value = steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(wl)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + desc + " (window setup untimed)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from partitioned_kv_cache_gb300 import rx
+
+    peaks, peak_kind = load_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed * 1000 + rank)
+
+    def randn_bf16(*shape, scale=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * scale).to(torch.bfloat16)
+
+    L, S, Hq, Hkv, D, K = wl.L, wl.S, wl.Hq, wl.Hkv, wl.D, wl.steps
+    cache = rx.Cache(L, Hq, Hkv, D, wl.P, wl.N, wl.F, S)
+    if args.splits:
+        cache.set_attn_splits(args.splits)
+    cache.pin_prefix(randn_bf16(L, wl.P, Hkv, D), randn_bf16(L, wl.P, Hkv, D))
+
+    NSLOT = 2   # alternating input pools, each larger than L2
+    frames = [(randn_bf16(L, wl.F, Hkv, D), randn_bf16(L, wl.F, Hkv, D)) for _ in range(NSLOT)]
+    q = randn_bf16(NSLOT, K, L, S, Hq, D)
+    kd = randn_bf16(NSLOT, K, L, S, Hkv, D)
+    vd = randn_bf16(NSLOT, K, L, S, Hkv, D)
+    x = randn_bf16(NSLOT, K, L, 2, S, wl.d_model)
+    o = torch.empty_like(q)
+    y = torch.empty_like(x)
+    n_sets = 2 * L
+    W1 = randn_bf16(n_sets, wl.hidden, wl.cond_dim, scale=0.02)
+    b1 = randn_bf16(n_sets, wl.hidden, scale=0.02)
+    W2 = randn_bf16(n_sets, wl.d_model, wl.hidden, scale=0.02)
+    b2 = randn_bf16(n_sets, wl.d_model, scale=0.02)
+    tk = torch.tensor(W.timesteps(wl), device=dev)
+    state = (torch.rand(NSLOT, K, wl.state_dim, generator=g, device=dev) * 2 - 1).contiguous()
+    gamma = torch.empty((n_sets, K, wl.d_model), dtype=torch.float32, device=dev)
+    for t in range(wl.N):   # fill the window before timing (steady state)
+        cache.push_frame(*frames[t % NSLOT])
+
+    def tick(slot):
+        rx.ada_gamma(tk, state[slot], W1, b1, W2, b2, wl.emb_dim, out=gamma)
+        cache.push_frame(*frames[slot])
+        for k in range(K):
+            for l in range(L):
+                rx.adarmsnorm(x[slot, k, l, 0], gamma[2 * l, k], wl.eps, out=y[slot, k, l, 0])
+                cache.attend_suffix(l, q[slot, k, l], kd[slot, k, l], vd[slot, k, l], out=o[slot, k, l])
+                rx.adarmsnorm(x[slot, k, l, 1], gamma[2 * l + 1, k], wl.eps, out=y[slot, k, l, 1])
+
+    def attn_only(slot):
+        for k in range(K):
+            for l in range(L):
+                cache.attend_suffix(l, q[slot, k, l], kd[slot, k, l], vd[slot, k, l], out=o[slot, k, l])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for s in range(NSLOT):   # eager warm-up (first launches set kernel attributes)
+            tick(s)
+    torch.cuda.synchronize()
+    graphs = []
+    n0 = rx.launch_count()
+    for s in range(NSLOT):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            tick(s)
+        graphs.append(gr)
+    launches_per_tick = (rx.launch_count() - n0) // NSLOT
+    a_graph = torch.cuda.CUDAGraph()
+    n1 = rx.launch_count()
+    with torch.cuda.graph(a_graph, stream=stream):
+        attn_only(0)
+    attn_kernels_per_call = (rx.launch_count() - n1) / (K * L)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % NSLOT].replay()
+    torch.cuda.synchronize()
+    assert cache.check_device_error() == 0, "a kernel reported a device-side timeout"
+
+    # ---------------- timed region: K ticks ----------------
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % NSLOT].replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        dist.barrier()
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    total_steps = args.steps * K * world
+    value = total_steps / (ms / 1e3)
+
+    # ---------------- attention alone: per-launch time for the roofline ----------------
+    reps = max(3, min(50, args.steps // 10))
+    with torch.cuda.stream(stream):
+        a_graph.replay()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            a_graph.replay()
+        a1.record(stream)
+    a1.synchronize()
+    attn_us = a0.elapsed_time(a1) * 1e3 / (reps * K * L)
+    fl = attn_flops(wl)
+    achieved = fl / (attn_us * 1e-6) / 1e12
+    peak_tf = float(peaks["bf16_tflops"])
+
+    # ---------------- append and AdaRMSNorm bandwidth ----------------
+    kern = {}
+    nfr = max(2, int(np.ceil(2 * 129e6 / (2 * L * wl.F * Hkv * D * 2))))
+    pool = [(randn_bf16(L, wl.F, Hkv, D), randn_bf16(L, wl.F, Hkv, D)) for _ in range(nfr)]
+    with torch.cuda.stream(stream):
+        for fr in pool:
+            cache.push_frame(*fr)
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for fr in pool:
+            cache.push_frame(*fr)
+        b1.record(stream)
+    b1.synchronize()
+    app_us = b0.elapsed_time(b1) * 1e3 / nfr
+    app_bytes = 2.0 * 2 * L * wl.F * Hkv * D * 2
+    kern["ring_append"] = {"us": app_us, "bytes": app_bytes, "GB/s": app_bytes / app_us / 1e3,
+                           "frac_hbm": app_bytes / app_us / 1e3 / float(peaks["hbm_gbs"]),
+                           "note": "one push of all %d layers, frames rotate over %d buffers" % (L, nfr)}
+    rows_bw = S * L * 2 * 64
+    xs = [randn_bf16(rows_bw, wl.d_model) for _ in range(2)]
+    ys = torch.empty_like(xs[0])
+    with torch.cuda.stream(stream):
+        rx.adarmsnorm(xs[0], gamma[0, 0], wl.eps, out=ys)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(10):
+            rx.adarmsnorm(xs[i % 2], gamma[0, 0], wl.eps, out=ys)
+        c1.record(stream)
+    c1.synchronize()
+    nrm_us = c0.elapsed_time(c1) * 1e3 / 10
+    nrm_bytes = 2.0 * rows_bw * wl.d_model * 2
+    kern["adarmsnorm_bw_scale"] = {"us": nrm_us, "rows": rows_bw, "bytes": nrm_bytes,
+                                   "GB/s": nrm_bytes / nrm_us / 1e3,
+                                   "frac_hbm": nrm_bytes / nrm_us / 1e3 / float(peaks["hbm_gbs"])}
+    kern["attention"] = {"us_per_call": attn_us, "kernels_per_call": attn_kernels_per_call,
+                         "flops_per_call": fl, "TFLOP/s": achieved}
+    del pool, xs, ys
+
+    # ---------------- end to end through the API with host buffers ----------------
+    h_fk = torch.empty((L, wl.F, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    h_fv = torch.empty_like(h_fk).pin_memory()
+    h_fk.copy_(frames[0][0].cpu())
+    h_fv.copy_(frames[0][1].cpu())
+    h_x = x[0, 0, 0, 0].cpu().pin_memory()
+    h_state = state[0].cpu().pin_memory()
+    h_out = torch.empty((S, Hq, D), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(4, args.steps // 4)
+    h2d = (h_fk.numel() + h_fv.numel() + h_x.numel()) * 2 + h_state.numel() * 4
+    d2h = h_out.numel() * 2
+    with torch.cuda.stream(stream):
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(e2e_steps):
+            s = i % NSLOT
+            frames[s][0].copy_(h_fk, non_blocking=True)
+            frames[s][1].copy_(h_fv, non_blocking=True)
+            x[s, 0, 0, 0].copy_(h_x, non_blocking=True)
+            state[s].copy_(h_state, non_blocking=True)
+            graphs[s].replay()
+            h_out.copy_(o[s, K - 1, L - 1], non_blocking=True)
+        f1.record(stream)
+    f1.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    e2e_val = e2e_steps * K * world / (e2e_ms / 1e3)
+    assert cache.check_device_error() == 0, "a kernel reported a device-side timeout"
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, dt, desc = oracle_sample(wl, args.seed, args.cpu_steps)
+        cpu = {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": desc + " (%.1f s)" % dt}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(wl), "step": "one stream tick: gamma for all sites and "
+                   "steps, 1 ring append, %d denoising steps x %d layers x {AdaRMSNorm, attention, "
+                   "AdaRMSNorm}, one CUDA graph" % (K, L),
+                   "keys_per_query": wl.keys_full, "attn_splits": "auto" if not args.splits else args.splits,
+                   "l2": "inputs larger than L2: two alternating input pools of %.0f MB each; the "
+                         "%.1f MB per-layer K/V store is reused across the %d steps of a tick by design"
+                         % ((q[0].numel() + kd[0].numel() * 2 + x[0].numel()) * 2 / 1e6,
+                            wl.cached * Hkv * D * 4 / 1e6, K),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "kernel": "partitioned attention (split-KV kernel + merge), %.2f us per call, "
+                               "%.3g algorithmic FLOP per call (4*Hq*S*Lk*D)" % (attn_us, fl),
+                     "peak_kind": "%s bf16 dense burst" % peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches_per_tick * args.steps),
+        "clocks": clocks,
+        "kernels": kern,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="c3", choices=["c2", "c3", "c4"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=0, help="split-KV partitions (0 = automatic)")
+    ap.add_argument("--cpu-steps", type=int, default=10, help="denoising steps in the CPU sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * rx.h -- C ABI of the GB300 partitioned KV cache and attention library
+ * (librx.so, built for sm_103a).
+ *
+ * What it computes
+ * ----------------
+ * Streaming inference for flow-matching vision-language-action policies as
+ * described in "Reflex: Real-Time VLA Control through Streaming Inference":
+ *
+ *  - §III "System architecture": the attention context is split into a
+ *    pinned instruction prefix (computed once), a sliding history holding a
+ *    FIFO of N observation frames (each tick enqueues the newest frame and
+ *    evicts the oldest) and a dynamic flow-state suffix recomputed at every
+ *    denoising step.
+ *  - §III "Core formulas", Eq. (1): the suffix queries attend with one softmax
+ *    over the concatenation [K_pin; K_slide(t); K_dyn(k)] (values likewise);
+ *    Proposition A.1: the result equals full-batch attention.
+ *  - §III "Core formulas", Eq. (2): AdaRMSNorm(x, c) = x / RMS(x) * gamma(c),
+ *    gamma(c) = 1 + MLP(c), RMS with an FP32 mean of squares.
+ *  - §V "Key implementation": a statically preallocated, zero-initialised
+ *    ring buffer with a write pointer; add_new_prefix() reports evictions.
+ *
+ * "OxyGen: Unified KV Cache Management for Vision-Language-Action Models under
+ * Multi-Task Parallelism", §"Core method": several requests read one
+ * read-only prefill cache while each keeps its own appended KV (rx_attend_batch).
+ *
+ * Conventions
+ * -----------
+ *  - Every function returns an rx_status: 0 on success, negative on error.
+ *    No C++ exception crosses this boundary.  rx_last_error() gives a
+ *    thread-local message for the last failure on the calling thread.
+ *  - "bf16" buffers hold IEEE bfloat16 values, row-major in the stated shape,
+ *    densely packed.  Unless stated otherwise a pointer is DEVICE memory
+ *    owned by the caller, 16-byte aligned; the library only reads inputs
+ *    and writes outputs during the call's stream work and keeps no pointer
+ *    to them afterwards.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls enqueue work and return without synchronising, except
+ *    where stated.  Work for one cache must stay in stream order: the cache
+ *    owns one workspace and one device-side {head, valid} state.
+ *  - Shapes: L layers, Hq query heads, Hkv key/value heads (Hq = G*Hkv, G a
+ *    power of two <= 128; query head h reads key/value head h / G), head
+ *    dimension D in {64, 128, 256}.
+ */
+#ifndef RX_H
+#define RX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rx_status {
+  RX_OK = 0,
+  RX_ERR_ARG = -1,         /* null/misaligned pointer, bad shape or size    */
+  RX_ERR_LAYER = -2,       /* layer index outside [0, L)                    */
+  RX_ERR_CAPACITY = -3,    /* P > P_cap, S > S_cap, tail > tail_cap, ...    */
+  RX_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed             */
+  RX_ERR_TIMEOUT = -5,     /* a bounded device-side wait gave up            */
+  RX_ERR_UNSUPPORTED = -6, /* shape the kernels do not handle (D, G, GPU)   */
+  RX_ERR_STATE = -7        /* call made in an invalid state                 */
+} rx_status;
+
+/* Opaque store: owns the pinned and sliding regions of every layer, the
+ * device-side ring state and the attention workspace, all in one device
+ * allocation made by rx_cache_create. */
+typedef struct rx_cache* rx_cache_t;
+
+typedef struct rx_config {
+  int L;        /* layers                                                   */
+  int Hq;       /* query heads                                              */
+  int Hkv;      /* key/value heads                                          */
+  int D;        /* head dimension: 64, 128 or 256                           */
+  int P_cap;    /* pinned-prefix capacity, tokens (>= 0)                    */
+  int N;        /* frames in the sliding window (>= 1)                      */
+  int F;        /* tokens per frame (>= 1)                                  */
+  int S_cap;    /* most query tokens of one attention call (>= 1)           */
+  int tail_cap; /* most private keys of one batched request (>= 0)          */
+  int max_req;  /* most requests of one rx_attend_batch call (>= 0)         */
+} rx_config;
+
+/* Allocate and zero every region ("Reflex ...", §V: the ring buffer is
+ * allocated once at model load with torch.zeros and a write pointer of 0).
+ * Device = the current CUDA device.  Synchronous.  On success *out owns the
+ * allocation until rx_cache_destroy.  Errors: RX_ERR_ARG (bad config),
+ * RX_ERR_UNSUPPORTED (D, G, or a GPU without sm_103a tcgen05), RX_ERR_CUDA. */
+rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out);
+
+/* Free everything the cache owns.  Synchronises the device first.  NULL is a
+ * no-op. */
+rx_status rx_cache_destroy(rx_cache_t cache);
+
+/* Copy the instruction prefix into the pinned region ("Reflex ...", §III
+ * Eq. 1 where-clause: K_pin, V_pin are computed once at t = 0 and pinned).
+ * k, v: bf16 [L][P][Hkv][D], host or device memory (copied with
+ * cudaMemcpyDefault, stream-ordered).  0 <= P <= P_cap.  Re-pinning replaces
+ * the prefix.  Errors: RX_ERR_ARG, RX_ERR_CAPACITY, RX_ERR_CUDA. */
+rx_status rx_pin_prefix(rx_cache_t cache, const void* k, const void* v, int P,
+                        void* stream);
+
+/* Ring append ("Reflex ...", §III "System architecture", sliding history;
+ * §V add_new_prefix / evict_source_prefix): for every layer write one frame's
+ * K/V into the slot at the device-side head, then head <- (head+1) mod N and
+ * valid <- min(valid+1, N).  Only the new frame is moved: O(L*F*Hkv*D) bytes,
+ * independent of N.  k, v: bf16 [L][F][Hkv][D], device memory.
+ * evicted (host, nullable): 1 if this push overwrote the oldest frame, else 0,
+ * from the host's count of pushes made through this function.
+ * Errors: RX_ERR_ARG, RX_ERR_CUDA. */
+rx_status rx_push_frame(rx_cache_t cache, const void* k, const void* v,
+                        int* evicted, void* stream);
+
+/* Partitioned attention for one layer ("Reflex ...", §III Eq. 1): for every
+ * suffix token s and query head h,
+ *   out[s][h] = softmax_j( q[s][h] . K_j / sqrt(D) ) V_j
+ * over all keys j of [pinned P; the window's valid*F frame tokens; k_dyn S],
+ * key/value head h / G.  No mask.  The window is read in place in physical
+ * slot order (softmax is order-invariant, Proposition A.1).
+ * q: bf16 [S][Hq][D]; k_dyn, v_dyn: bf16 [S][Hkv][D]; out: bf16 [S][Hq][D];
+ * 1 <= S <= S_cap.  fp32 accumulation and softmax; out rounded once to bf16.
+ * Errors: RX_ERR_ARG, RX_ERR_LAYER, RX_ERR_CAPACITY, RX_ERR_CUDA. */
+rx_status rx_attend_suffix(rx_cache_t cache, int layer, const void* q,
+                           const void* k_dyn, const void* v_dyn, int S,
+                           void* out, void* stream);
+
+/* One request of a batched shared-cache call. */
+typedef struct rx_request {
+  const void* q;      /* bf16 [n_tok][Hq][D]                                 */
+  const void* k_priv; /* bf16 [n_priv][Hkv][D], this request's own keys      */
+  const void* v_priv; /* bf16 [n_priv][Hkv][D]                               */
+  void* out;          /* bf16 [n_tok][Hq][D]                                 */
+  int n_tok;          /* query tokens, >= 1                                  */
+  int n_priv;         /* private keys, >= 0                                  */
+} rx_request;
+
+/* Shared-cache multi-request attention in one launch ("OxyGen ...",
+ * §"Core method", cross-task KV sharing): every request attends over the
+ * layer's read-only [pinned; window] plus only its own private keys (the
+ * action suffix's k_dyn, or a language stream's appended tail).  Nothing one
+ * request supplies enters another's softmax.  reqs: HOST array of nreq
+ * entries whose pointers are device memory.  Limits: sum over requests of
+ * n_tok <= S_cap + max_req, each n_priv <= max(S_cap, tail_cap),
+ * nreq <= max_req + 1.  Errors as rx_attend_suffix. */
+rx_status rx_attend_batch(rx_cache_t cache, int layer, const rx_request* reqs,
+                          int nreq, void* stream);
+
+/* Gamma of AdaRMSNorm ("Reflex ...", §III Eq. 2 and "Model components"):
+ * for every weight set i and conditioning vector k
+ *   c_k      = [sin(t_k w_0..), cos(t_k w_0..), state_k]   (emb_dim + state_dim)
+ *   w_j      = 10000^(-j / (emb_dim/2)),  j < emb_dim/2
+ *   gamma[i][k] = 1 + W2_i SiLU(W1_i c_k + b1_i) + b2_i
+ * t: fp32 [n_cond]; state: fp32 [n_cond][state_dim];
+ * W1: bf16 [n_sets][hidden][emb_dim+state_dim]; b1: bf16 [n_sets][hidden];
+ * W2: bf16 [n_sets][d][hidden]; b2: bf16 [n_sets][d];
+ * gamma: fp32 [n_sets][n_cond][d] (output).  bf16 weights, fp32 arithmetic.
+ * Limits: 1 <= n_cond <= 16, emb_dim even, hidden <= 2048, d % 8 == 0.
+ * Errors: RX_ERR_ARG, RX_ERR_CUDA. */
+rx_status rx_ada_gamma(const float* t, const float* state, int n_cond,
+                       int emb_dim, int state_dim, const void* W1,
+                       const void* b1, int hidden, const void* W2,
+                       const void* b2, int d, int n_sets, float* gamma,
+                       void* stream);
+
+/* AdaRMSNorm ("Reflex ...", §III Eq. 2; §V forward): for each row
+ *   y = x * rsqrt(mean(x^2) + eps) * gamma
+ * with the mean of squares accumulated in fp32.  x, y: bf16 [rows][d];
+ * gamma: fp32 [d]; d % 8 == 0; rows >= 0 (0 is a no-op).  y may not alias x.
+ * Errors: RX_ERR_ARG, RX_ERR_CUDA. */
+rx_status rx_adarmsnorm(const void* x, const float* gamma, int rows, int d,
+                        float eps, void* y, void* stream);
+
+/* Read the device-side ring state (synchronises `stream`): head = slot the
+ * next push writes, valid = frames held, pushes = pushes applied on the
+ * device (advances under CUDA-graph replay too).  Any pointer may be NULL. */
+rx_status rx_get_state(rx_cache_t cache, int* head, int* valid,
+                       long long* pushes, void* stream);
+
+/* Test aid: the window's physical slots in logical order, oldest first
+ * (slots: host int[N], the first *valid entries are filled).  Reads the
+ * device state (synchronises `stream`). */
+rx_status rx_debug_window(rx_cache_t cache, int* slots, int* valid,
+                          void* stream);
+
+/* Test aid: copy one layer's window in logical order (oldest frame first)
+ * into k_out, v_out: device bf16 [valid*F][Hkv][D].  Reads the device state
+ * (synchronises `stream`), then enqueues the copies. */
+rx_status rx_export_window(rx_cache_t cache, int layer, void* k_out,
+                           void* v_out, void* stream);
+
+/* Device-side error word of the cache (bit flags set by kernels whose bounded
+ * waits gave up).  Synchronises `stream`; *code = 0 means no error.  The word
+ * is cleared by this call. */
+rx_status rx_check_device_error(rx_cache_t cache, int* code, void* stream);
+
+/* Number of split-KV partitions for attention launches of this cache
+ * (0 = chosen from the SM count, the default).  A tuning knob: results are
+ * the same for every value up to rounding order. */
+rx_status rx_set_attn_splits(rx_cache_t cache, int splits);
+
+/* Kernel launches made by the library in this process (all entry points,
+ * all caches).  For accounting in benchmarks. */
+long long rx_launch_count(void);
+
+const char* rx_status_str(int status);
+const char* rx_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RX_H */

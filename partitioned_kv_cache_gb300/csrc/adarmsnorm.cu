@@ -1,0 +1,242 @@
+// adarmsnorm.cu -- AdaRMSNorm and its conditioning gate.
+//
+// "Reflex: Real-Time VLA Control through Streaming Inference", §III "Core
+// formulas", Eq. (2):
+//   AdaRMSNorm(x, c) = x / RMS(x) * gamma(c),  gamma(c) = 1 + MLP(c),
+//   RMS(x) = sqrt(mean_i x_i^2 + eps)
+// with c = [sinusoidal t_k; robot state s_t].  The mean of squares is taken in
+// FP32 (the page's remedy for bf16 underflow); the MLP is
+// Linear(cond -> hidden) -> SiLU -> Linear(hidden -> d) ("Model components"),
+// run here with bf16 weights and fp32 arithmetic.
+//
+// gamma depends only on (t_k, s_t) and the site's weights, never on x, so one
+// launch computes every (weight set, conditioning vector) pair of a tick up
+// front; the norm itself is one warp per row with 16-byte bf16 vectors.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "rx_internal.h"
+
+namespace rx {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp per row.  MAXV = 16-byte vectors per lane kept in registers
+// (d <= 256 * MAXV); MAXV = 0 selects the two-pass path for wider rows.
+template <int MAXV>
+__global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict__ x,
+                                                         const float* __restrict__ gamma,
+                                                         int rows, int d, float eps,
+                                                         uint4* __restrict__ y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
+  if (row >= rows) return;
+  const int nv = d >> 3;
+  const uint4* xr = x + row * nv;
+  uint4* yr = y + row * nv;
+  const float inv_d = 1.0f / static_cast<float>(d);
+  if constexpr (MAXV > 0) {
+    uint4 xv[MAXV];
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u) {
+      const int v = lane + 32 * u;
+      if (v < nv) {
+        xv[u] = xr[v];
+        float f[8];
+        unpack8(xv[u], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+      }
+    }
+    const float r = rsqrtf(warp_sum(ss) * inv_d + eps);
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u) {
+      const int v = lane + 32 * u;
+      if (v < nv) {
+        float f[8];
+        unpack8(xv[u], f);
+        const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * v);
+        const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * v + 4);
+        yr[v] = make_uint4(pack2(f[0] * r * g0.x, f[1] * r * g0.y),
+                           pack2(f[2] * r * g0.z, f[3] * r * g0.w),
+                           pack2(f[4] * r * g1.x, f[5] * r * g1.y),
+                           pack2(f[6] * r * g1.z, f[7] * r * g1.w));
+      }
+    }
+  } else {
+    float ss = 0.f;
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      unpack8(xr[v], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+    const float r = rsqrtf(warp_sum(ss) * inv_d + eps);
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      unpack8(xr[v], f);
+      const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * v);
+      const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * v + 4);
+      yr[v] = make_uint4(pack2(f[0] * r * g0.x, f[1] * r * g0.y),
+                         pack2(f[2] * r * g0.z, f[3] * r * g0.w),
+                         pack2(f[4] * r * g1.x, f[5] * r * g1.y),
+                         pack2(f[6] * r * g1.z, f[7] * r * g1.w));
+    }
+  }
+}
+
+constexpr int kGammaRows = 64;   // output rows of gamma per CTA
+
+// grid (ceil(d / 64), n_sets), 256 threads.  Shared: c [n_cond][cond_dim] and
+// the hidden activations h [n_cond][hidden].  Every CTA of a weight set
+// recomputes h; W1 (hidden x cond_dim) is small and stays in L2.
+__global__ void __launch_bounds__(256) ada_gamma_kernel(
+    const float* __restrict__ t, const float* __restrict__ state, int n_cond, int emb_dim,
+    int state_dim, const __nv_bfloat16* __restrict__ W1, const __nv_bfloat16* __restrict__ b1,
+    int hidden, const __nv_bfloat16* __restrict__ W2, const __nv_bfloat16* __restrict__ b2,
+    int d, float* __restrict__ gamma) {
+  extern __shared__ float sh[];
+  const int cond_dim = emb_dim + state_dim;
+  float* c = sh;                        // [n_cond][cond_dim]
+  float* h = sh + n_cond * cond_dim;    // [n_cond][hidden]
+  const int set = blockIdx.y;
+  const int half = emb_dim / 2;
+
+  // c_k = [sin(t_k w_j), cos(t_k w_j), state_k],  w_j = 10000^(-j/half)
+  for (int idx = threadIdx.x; idx < n_cond * cond_dim; idx += blockDim.x) {
+    const int k = idx / cond_dim, j = idx - k * cond_dim;
+    float v;
+    if (j < emb_dim) {
+      const int jj = j < half ? j : j - half;
+      const float w = powf(10000.0f, -static_cast<float>(jj) / static_cast<float>(half));
+      v = j < half ? sinf(t[k] * w) : cosf(t[k] * w);
+    } else {
+      v = state[k * state_dim + (j - emb_dim)];
+    }
+    c[idx] = v;
+  }
+  __syncthreads();
+
+  // h_k = SiLU(W1 c_k + b1)
+  const __nv_bfloat16* W1s = W1 + static_cast<size_t>(set) * hidden * cond_dim;
+  const __nv_bfloat16* b1s = b1 + static_cast<size_t>(set) * hidden;
+  for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
+    float acc[kMaxCond];
+#pragma unroll
+    for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
+    const __nv_bfloat16* wr = W1s + static_cast<size_t>(j) * cond_dim;
+    for (int e = 0; e < cond_dim; ++e) {
+      const float w = __bfloat162float(wr[e]);
+#pragma unroll
+      for (int k = 0; k < kMaxCond; ++k)
+        if (k < n_cond) acc[k] = fmaf(w, c[k * cond_dim + e], acc[k]);
+    }
+    const float bias = __bfloat162float(b1s[j]);
+#pragma unroll
+    for (int k = 0; k < kMaxCond; ++k) {
+      if (k < n_cond) {
+        const float z = acc[k] + bias;
+        h[k * hidden + j] = z / (1.0f + expf(-z));
+      }
+    }
+  }
+  __syncthreads();
+
+  // gamma_k[i] = 1 + W2[i] . h_k + b2[i]: one warp per output row.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16* W2s = W2 + static_cast<size_t>(set) * d * hidden;
+  const __nv_bfloat16* b2s = b2 + static_cast<size_t>(set) * d;
+  const int row_end = min(d, (blockIdx.x + 1) * kGammaRows);
+  const int nvh = hidden >> 3;
+  for (int i = blockIdx.x * kGammaRows + warp; i < row_end; i += 8) {
+    float acc[kMaxCond];
+#pragma unroll
+    for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
+    const uint4* wr = reinterpret_cast<const uint4*>(W2s + static_cast<size_t>(i) * hidden);
+    for (int v = lane; v < nvh; v += 32) {
+      float w[8];
+      unpack8(wr[v], w);
+#pragma unroll
+      for (int k = 0; k < kMaxCond; ++k) {
+        if (k < n_cond) {
+          const float* hk = h + k * hidden + 8 * v;
+          float a = acc[k];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a = fmaf(w[e], hk[e], a);
+          acc[k] = a;
+        }
+      }
+    }
+    const float bias = __bfloat162float(b2s[i]);
+#pragma unroll
+    for (int k = 0; k < kMaxCond; ++k) {
+      if (k < n_cond) {
+        const float s = warp_sum(acc[k]);
+        if (lane == 0) gamma[(static_cast<size_t>(set) * n_cond + k) * d + i] = 1.0f + s + bias;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_adarmsnorm(const __nv_bfloat16* x, const float* gamma, int rows, int d,
+                              float eps, __nv_bfloat16* y, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const unsigned int blocks = static_cast<unsigned int>((rows + 7) / 8);
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4* yv = reinterpret_cast<uint4*>(y);
+  if (d <= 256)
+    adarmsnorm_kernel<1><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+  else if (d <= 512)
+    adarmsnorm_kernel<2><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+  else if (d <= 1024)
+    adarmsnorm_kernel<4><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+  else if (d <= 2048)
+    adarmsnorm_kernel<8><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+  else
+    adarmsnorm_kernel<0><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int emb_dim,
+                             int state_dim, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
+                             int hidden, const __nv_bfloat16* W2, const __nv_bfloat16* b2, int d,
+                             int n_sets, float* gamma, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(n_cond) * (emb_dim + state_dim + hidden) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(ada_gamma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((d + kGammaRows - 1) / kGammaRows, n_sets);
+  ada_gamma_kernel<<<grid, 256, smem, s>>>(t, state, n_cond, emb_dim, state_dim, W1, b1, hidden,
+                                            W2, b2, d, gamma);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace rx

@@ -1,0 +1,497 @@
+// rx_api.cu -- host side of the C ABI declared in include/rx.h.
+//
+// The store object ("Reflex: Real-Time VLA Control through Streaming
+// Inference", §V "Key implementation": a statically preallocated,
+// zero-initialised ring buffer with a write pointer) owns one device
+// allocation holding, per layer, the pinned region [P_cap][Hkv][D] and the
+// window [N][F][Hkv][D] for K and V, the device-side ring state and the
+// split-KV workspace of the attention kernel.  Every entry point validates its
+// arguments on the host, returns an rx_status and never throws.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "rx.h"
+#include "rx_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<long long> g_launches{0};
+
+rx_status fail(rx_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+rx_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RX_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+namespace rx {
+
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_tmap_4d(CUtensorMap* tm, const void* base, const uint64_t dims[4],
+                    const uint64_t strides_bytes[3], const uint32_t box[4]) {
+  EncodeTiledFn f = encode_tiled();
+  if (!f) return false;
+  cuuint64_t gd[4], gs[3];
+  cuuint32_t bx[4], es[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 4; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i < 3; ++i) gs[i] = strides_bytes[i];
+  const CUresult r =
+      f(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, bx, es,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace rx
+
+struct rx_cache {
+  rx_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  void* mem = nullptr;
+  size_t mem_bytes = 0;
+  __nv_bfloat16* k_pin = nullptr;
+  __nv_bfloat16* v_pin = nullptr;
+  __nv_bfloat16* k_win = nullptr;
+  __nv_bfloat16* v_win = nullptr;
+  rx::DevState* dstate = nullptr;
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  int max_splits = 0;
+  int pin_rows = 0;      // allocated pinned rows per layer: max(P_cap, 1)
+  int P = 0;             // pinned tokens currently held
+  long long host_pushes = 0;
+  int forced_splits = 0;
+  CUtensorMap tm_pin_k, tm_pin_v, tm_win_k, tm_win_v;
+};
+
+#define RX_GUARD_BEGIN try {
+#define RX_GUARD_END                                              \
+  }                                                               \
+  catch (const std::bad_alloc&) {                                 \
+    return fail(RX_ERR_ARG, "host allocation failed");            \
+  }                                                               \
+  catch (...) {                                                   \
+    return fail(RX_ERR_ARG, "unexpected host exception");         \
+  }
+
+extern "C" {
+
+const char* rx_status_str(int s) {
+  switch (s) {
+    case RX_OK: return "RX_OK";
+    case RX_ERR_ARG: return "RX_ERR_ARG";
+    case RX_ERR_LAYER: return "RX_ERR_LAYER";
+    case RX_ERR_CAPACITY: return "RX_ERR_CAPACITY";
+    case RX_ERR_CUDA: return "RX_ERR_CUDA";
+    case RX_ERR_TIMEOUT: return "RX_ERR_TIMEOUT";
+    case RX_ERR_UNSUPPORTED: return "RX_ERR_UNSUPPORTED";
+    case RX_ERR_STATE: return "RX_ERR_STATE";
+    default: return "RX_ERR_UNKNOWN";
+  }
+}
+
+const char* rx_last_error(void) { return g_last_error.c_str(); }
+
+long long rx_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
+  RX_GUARD_BEGIN
+  if (!cfg || !out) return fail(RX_ERR_ARG, "rx_cache_create: null argument");
+  *out = nullptr;
+  const rx_config& c = *cfg;
+  if (c.L < 1 || c.Hq < 1 || c.Hkv < 1 || c.N < 1 || c.F < 1 || c.S_cap < 1 || c.P_cap < 0 ||
+      c.tail_cap < 0 || c.max_req < 0)
+    return fail(RX_ERR_ARG, "rx_cache_create: sizes out of range");
+  if (c.Hq % c.Hkv) return fail(RX_ERR_ARG, "rx_cache_create: Hq must be a multiple of Hkv");
+  const int G = c.Hq / c.Hkv;
+  if (!pow2(G) || G > rx::kBM)
+    return fail(RX_ERR_UNSUPPORTED, "rx_cache_create: Hq/Hkv = %d must be a power of two <= 128", G);
+  if (c.D != 64 && c.D != 128 && c.D != 256)
+    return fail(RX_ERR_UNSUPPORTED, "rx_cache_create: head dim %d not in {64, 128, 256}", c.D);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(RX_ERR_UNSUPPORTED, "rx_cache_create: device is sm_%d%d, the kernels are built for sm_103a",
+                prop.major, prop.minor);
+
+  rx_cache* h = new rx_cache();
+  h->cfg = c;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->max_splits = h->num_sms < 64 ? h->num_sms : 64;
+  h->pin_rows = c.P_cap > 0 ? c.P_cap : 1;
+
+  const size_t tok = static_cast<size_t>(c.Hkv) * c.D * 2;   // bytes per token
+  const size_t pin_b = round_up(static_cast<size_t>(c.L) * h->pin_rows * tok, 256);
+  const size_t win_b = round_up(static_cast<size_t>(c.L) * c.N * c.F * tok, 256);
+  const int max_tok = c.S_cap > c.tail_cap ? c.S_cap : c.tail_cap;
+  const size_t rows_pad = round_up(static_cast<size_t>(max_tok) * G, rx::kBM);
+  const size_t part_rows = static_cast<size_t>(c.Hkv) * h->max_splits * rows_pad;
+  const size_t po_b = round_up(part_rows * c.D * sizeof(float), 256);
+  const size_t pml_b = round_up(part_rows * sizeof(float2), 256);
+  const size_t st_b = 256;
+  h->mem_bytes = 2 * pin_b + 2 * win_b + st_b + po_b + pml_b;
+  e = cudaMalloc(&h->mem, h->mem_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "rx_cache_create: cudaMalloc");
+  }
+  e = cudaMemset(h->mem, 0, h->mem_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->mem);
+    delete h;
+    return cuda_fail(e, "rx_cache_create: cudaMemset");
+  }
+  char* p = static_cast<char*>(h->mem);
+  h->k_pin = reinterpret_cast<__nv_bfloat16*>(p); p += pin_b;
+  h->v_pin = reinterpret_cast<__nv_bfloat16*>(p); p += pin_b;
+  h->k_win = reinterpret_cast<__nv_bfloat16*>(p); p += win_b;
+  h->v_win = reinterpret_cast<__nv_bfloat16*>(p); p += win_b;
+  h->dstate = reinterpret_cast<rx::DevState*>(p); p += st_b;
+  h->part_o = reinterpret_cast<float*>(p); p += po_b;
+  h->part_ml = reinterpret_cast<float2*>(p);
+
+  // Tensor maps of the two cached regions, all layers: (D, Hkv, tokens, L).
+  bool ok = true;
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(c.D), static_cast<uint64_t>(c.Hkv),
+                              static_cast<uint64_t>(h->pin_rows), static_cast<uint64_t>(c.L)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(c.D) * 2, tok, h->pin_rows * tok};
+    const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
+    ok = ok && rx::encode_tmap_4d(&h->tm_pin_k, h->k_pin, dims, strides, box);
+    ok = ok && rx::encode_tmap_4d(&h->tm_pin_v, h->v_pin, dims, strides, box);
+  }
+  {
+    const uint64_t wt = static_cast<uint64_t>(c.N) * c.F;
+    const uint64_t dims[4] = {static_cast<uint64_t>(c.D), static_cast<uint64_t>(c.Hkv), wt,
+                              static_cast<uint64_t>(c.L)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(c.D) * 2, tok, wt * tok};
+    const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
+    ok = ok && rx::encode_tmap_4d(&h->tm_win_k, h->k_win, dims, strides, box);
+    ok = ok && rx::encode_tmap_4d(&h->tm_win_v, h->v_win, dims, strides, box);
+  }
+  if (!ok) {
+    cudaFree(h->mem);
+    delete h;
+    return fail(RX_ERR_CUDA, "rx_cache_create: tensor-map encoding failed");
+  }
+  *out = h;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_cache_destroy(rx_cache_t h) {
+  RX_GUARD_BEGIN
+  if (!h) return RX_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t e2 = cudaFree(h->mem);
+  delete h;
+  if (e != cudaSuccess) return cuda_fail(e, "rx_cache_destroy: synchronize");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "rx_cache_destroy: cudaFree");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_pin_prefix(rx_cache_t h, const void* k, const void* v, int P, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_pin_prefix: null cache");
+  const rx_config& c = h->cfg;
+  if (P < 0) return fail(RX_ERR_ARG, "rx_pin_prefix: P < 0");
+  if (P > c.P_cap) return fail(RX_ERR_CAPACITY, "rx_pin_prefix: P = %d > P_cap = %d", P, c.P_cap);
+  if (P > 0 && (!k || !v)) return fail(RX_ERR_ARG, "rx_pin_prefix: null K/V");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (P > 0) {
+    const size_t tok = static_cast<size_t>(c.Hkv) * c.D * 2;
+    const size_t width = static_cast<size_t>(P) * tok;
+    const size_t dpitch = static_cast<size_t>(h->pin_rows) * tok;
+    cudaError_t e = cudaMemcpy2DAsync(h->k_pin, dpitch, k, width, width, c.L, cudaMemcpyDefault, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(h->v_pin, dpitch, v, width, width, c.L, cudaMemcpyDefault, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rx_pin_prefix: copy");
+  }
+  h->P = P;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_push_frame(rx_cache_t h, const void* k, const void* v, int* evicted, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_push_frame: null cache");
+  if (!k || !v) return fail(RX_ERR_ARG, "rx_push_frame: null K/V");
+  if (!aligned16(k) || !aligned16(v)) return fail(RX_ERR_ARG, "rx_push_frame: K/V not 16-byte aligned");
+  const rx_config& c = h->cfg;
+  const long long frame_bytes = static_cast<long long>(c.F) * c.Hkv * c.D * 2;
+  cudaError_t e = rx::launch_ring_append(k, v, h->k_win, h->v_win, h->dstate, c.L, c.N,
+                                         frame_bytes, h->num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rx_push_frame: launch");
+  if (evicted) *evicted = h->host_pushes >= c.N ? 1 : 0;
+  h->host_pushes += 1;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
+  rx::AttnLaunch a;
+  a.tm_pin_k = &h->tm_pin_k;
+  a.tm_pin_v = &h->tm_pin_v;
+  a.tm_slide_k = &h->tm_win_k;
+  a.tm_slide_v = &h->tm_win_v;
+  a.layer = layer;
+  a.P = h->P;
+  a.F = h->cfg.F;
+  a.N = h->cfg.N;
+  a.D = h->cfg.D;
+  a.Hq = h->cfg.Hq;
+  a.Hkv = h->cfg.Hkv;
+  a.st = h->dstate;
+  a.err = &h->dstate->err;
+  a.part_o = h->part_o;
+  a.part_ml = h->part_ml;
+  a.max_splits = h->max_splits;
+  a.forced_splits = h->forced_splits;
+  a.num_sms = h->num_sms;
+  return a;
+}
+
+rx_status rx_attend_suffix(rx_cache_t h, int layer, const void* q, const void* k_dyn,
+                           const void* v_dyn, int S, void* out, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_attend_suffix: null cache");
+  const rx_config& c = h->cfg;
+  if (layer < 0 || layer >= c.L) return fail(RX_ERR_LAYER, "rx_attend_suffix: layer %d not in [0, %d)", layer, c.L);
+  if (S < 1) return fail(RX_ERR_ARG, "rx_attend_suffix: S < 1");
+  if (S > c.S_cap) return fail(RX_ERR_CAPACITY, "rx_attend_suffix: S = %d > S_cap = %d", S, c.S_cap);
+  if (!q || !k_dyn || !v_dyn || !out) return fail(RX_ERR_ARG, "rx_attend_suffix: null pointer");
+  if (!aligned16(q) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out))
+    return fail(RX_ERR_ARG, "rx_attend_suffix: pointers must be 16-byte aligned");
+  const rx::AttnLaunch a = make_launch(h, layer);
+  rx::AttnRequest r{q, k_dyn, v_dyn, out, S, S};
+  cudaError_t e = rx::launch_partitioned_attention(a, &r, 1, static_cast<cudaStream_t>(stream), nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_attend_suffix: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_attend_batch(rx_cache_t h, int layer, const rx_request* reqs, int nreq, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_attend_batch: null cache");
+  const rx_config& c = h->cfg;
+  if (layer < 0 || layer >= c.L) return fail(RX_ERR_LAYER, "rx_attend_batch: layer %d not in [0, %d)", layer, c.L);
+  if (nreq < 0 || (nreq > 0 && !reqs)) return fail(RX_ERR_ARG, "rx_attend_batch: bad request array");
+  if (nreq > c.max_req + 1 || nreq > rx::kMaxReq)
+    return fail(RX_ERR_CAPACITY, "rx_attend_batch: %d requests > max_req + 1 = %d", nreq, c.max_req + 1);
+  const int priv_cap = c.S_cap > c.tail_cap ? c.S_cap : c.tail_cap;
+  long long tot = 0;
+  rx::AttnRequest rr[rx::kMaxReq];
+  for (int i = 0; i < nreq; ++i) {
+    const rx_request& r = reqs[i];
+    if (r.n_tok < 1 || r.n_priv < 0) return fail(RX_ERR_ARG, "rx_attend_batch: request %d sizes", i);
+    if (r.n_tok > priv_cap) return fail(RX_ERR_CAPACITY, "rx_attend_batch: request %d n_tok = %d too large", i, r.n_tok);
+    if (r.n_priv > priv_cap) return fail(RX_ERR_CAPACITY, "rx_attend_batch: request %d n_priv = %d > %d", i, r.n_priv, priv_cap);
+    if (!r.q || !r.out || (r.n_priv > 0 && (!r.k_priv || !r.v_priv)))
+      return fail(RX_ERR_ARG, "rx_attend_batch: request %d null pointer", i);
+    if (!aligned16(r.q) || !aligned16(r.out) || (r.n_priv > 0 && (!aligned16(r.k_priv) || !aligned16(r.v_priv))))
+      return fail(RX_ERR_ARG, "rx_attend_batch: request %d pointers must be 16-byte aligned", i);
+    tot += r.n_tok;
+    rr[i] = rx::AttnRequest{r.q, r.k_priv, r.v_priv, r.out, r.n_tok, r.n_priv};
+  }
+  if (tot > static_cast<long long>(c.S_cap) + c.max_req)
+    return fail(RX_ERR_CAPACITY, "rx_attend_batch: %lld query tokens > S_cap + max_req", tot);
+  if (nreq == 0) return RX_OK;
+  const rx::AttnLaunch a = make_launch(h, layer);
+  cudaError_t e = rx::launch_partitioned_attention(a, rr, nreq, static_cast<cudaStream_t>(stream), nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_attend_batch: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_ada_gamma(const float* t, const float* state, int n_cond, int emb_dim, int state_dim,
+                       const void* W1, const void* b1, int hidden, const void* W2, const void* b2,
+                       int d, int n_sets, float* gamma, void* stream) {
+  RX_GUARD_BEGIN
+  if (n_cond < 1 || n_cond > rx::kMaxCond)
+    return fail(RX_ERR_ARG, "rx_ada_gamma: n_cond = %d not in [1, %d]", n_cond, rx::kMaxCond);
+  if (emb_dim < 0 || (emb_dim & 1) || state_dim < 0 || emb_dim + state_dim < 1)
+    return fail(RX_ERR_ARG, "rx_ada_gamma: emb_dim must be even, widths >= 0, cond width >= 1");
+  if (hidden < 8 || hidden > rx::kMaxHidden || (hidden & 7))
+    return fail(RX_ERR_ARG, "rx_ada_gamma: hidden = %d must be a multiple of 8 in [8, %d]", hidden, rx::kMaxHidden);
+  if (d < 8 || (d & 7)) return fail(RX_ERR_ARG, "rx_ada_gamma: d = %d must be a positive multiple of 8", d);
+  if (n_sets < 1) return fail(RX_ERR_ARG, "rx_ada_gamma: n_sets < 1");
+  if (!t || (state_dim > 0 && !state) || !W1 || !b1 || !W2 || !b2 || !gamma)
+    return fail(RX_ERR_ARG, "rx_ada_gamma: null pointer");
+  if (!aligned16(W2) || (reinterpret_cast<uintptr_t>(W1) & 1) || (reinterpret_cast<uintptr_t>(b1) & 1) ||
+      (reinterpret_cast<uintptr_t>(b2) & 1) || (reinterpret_cast<uintptr_t>(gamma) & 3) ||
+      (reinterpret_cast<uintptr_t>(t) & 3) || (reinterpret_cast<uintptr_t>(state) & 3))
+    return fail(RX_ERR_ARG, "rx_ada_gamma: misaligned pointer");
+  cudaError_t e = rx::launch_ada_gamma(t, state, n_cond, emb_dim, state_dim,
+                                       static_cast<const __nv_bfloat16*>(W1),
+                                       static_cast<const __nv_bfloat16*>(b1), hidden,
+                                       static_cast<const __nv_bfloat16*>(W2),
+                                       static_cast<const __nv_bfloat16*>(b2), d, n_sets, gamma,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rx_ada_gamma: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_adarmsnorm(const void* x, const float* gamma, int rows, int d, float eps, void* y,
+                        void* stream) {
+  RX_GUARD_BEGIN
+  if (rows < 0) return fail(RX_ERR_ARG, "rx_adarmsnorm: rows < 0");
+  if (d < 8 || (d & 7)) return fail(RX_ERR_ARG, "rx_adarmsnorm: d = %d must be a positive multiple of 8", d);
+  if (!(eps >= 0.f)) return fail(RX_ERR_ARG, "rx_adarmsnorm: eps must be >= 0");
+  if (rows == 0) return RX_OK;
+  if (!x || !gamma || !y) return fail(RX_ERR_ARG, "rx_adarmsnorm: null pointer");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma))
+    return fail(RX_ERR_ARG, "rx_adarmsnorm: pointers must be 16-byte aligned");
+  if (x == y) return fail(RX_ERR_ARG, "rx_adarmsnorm: y may not alias x");
+  cudaError_t e = rx::launch_adarmsnorm(static_cast<const __nv_bfloat16*>(x), gamma, rows, d, eps,
+                                        static_cast<__nv_bfloat16*>(y),
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rx_adarmsnorm: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+static rx_status read_state(rx_cache_t h, rx::DevState* ds, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(ds, h->dstate, sizeof(*ds), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading device ring state");
+  return RX_OK;
+}
+
+rx_status rx_get_state(rx_cache_t h, int* head, int* valid, long long* pushes, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_get_state: null cache");
+  rx::DevState ds;
+  rx_status r = read_state(h, &ds, static_cast<cudaStream_t>(stream));
+  if (r != RX_OK) return r;
+  if (head) *head = ds.head;
+  if (valid) *valid = ds.valid;
+  if (pushes) *pushes = ds.pushes;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_debug_window(rx_cache_t h, int* slots, int* valid, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h || !slots || !valid) return fail(RX_ERR_ARG, "rx_debug_window: null argument");
+  rx::DevState ds;
+  rx_status r = read_state(h, &ds, static_cast<cudaStream_t>(stream));
+  if (r != RX_OK) return r;
+  const int N = h->cfg.N;
+  const int oldest = ((ds.head - ds.valid) % N + N) % N;
+  for (int i = 0; i < ds.valid; ++i) slots[i] = (oldest + i) % N;
+  *valid = ds.valid;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_export_window(rx_cache_t h, int layer, void* k_out, void* v_out, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h || !k_out || !v_out) return fail(RX_ERR_ARG, "rx_export_window: null argument");
+  const rx_config& c = h->cfg;
+  if (layer < 0 || layer >= c.L) return fail(RX_ERR_LAYER, "rx_export_window: layer %d", layer);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int slots[4096];
+  if (c.N > 4096) return fail(RX_ERR_UNSUPPORTED, "rx_export_window: N > 4096");
+  int valid = 0;
+  rx_status r = rx_debug_window(h, slots, &valid, stream);
+  if (r != RX_OK) return r;
+  const size_t fb = static_cast<size_t>(c.F) * c.Hkv * c.D * 2;
+  for (int i = 0; i < valid; ++i) {
+    const size_t src = (static_cast<size_t>(layer) * c.N + slots[i]) * fb;
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(k_out) + i * fb,
+                                    reinterpret_cast<char*>(h->k_win) + src, fb,
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(v_out) + i * fb,
+                          reinterpret_cast<char*>(h->v_win) + src, fb, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rx_export_window: copy");
+  }
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_check_device_error(rx_cache_t h, int* code, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h || !code) return fail(RX_ERR_ARG, "rx_check_device_error: null argument");
+  rx::DevState ds;
+  rx_status r = read_state(h, &ds, static_cast<cudaStream_t>(stream));
+  if (r != RX_OK) return r;
+  *code = ds.err;
+  if (ds.err) {
+    cudaError_t e = cudaMemsetAsync(&h->dstate->err, 0, sizeof(int), static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rx_check_device_error: clear");
+  }
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_set_attn_splits(rx_cache_t h, int splits) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_set_attn_splits: null cache");
+  if (splits < 0 || splits > h->max_splits)
+    return fail(RX_ERR_ARG, "rx_set_attn_splits: %d not in [0, %d]", splits, h->max_splits);
+  h->forced_splits = splits;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+}  // extern "C"

@@ -1,0 +1,230 @@
+"""Python binding of librx.so (the C ABI in include/rx.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  Import
+fails loudly when the library has not been built -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librx.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        "librx.so is not built (expected at %s); run `python -c \"import __graft_entry__ as g; "
+        "g.build()\"` or `python -m partitioned_kv_cache_gb300.build`" % _LIB_PATH)
+_lib = ctypes.CDLL(_LIB_PATH)
+
+RX_OK = 0
+STATUS_NAMES = {0: "RX_OK", -1: "RX_ERR_ARG", -2: "RX_ERR_LAYER", -3: "RX_ERR_CAPACITY",
+                -4: "RX_ERR_CUDA", -5: "RX_ERR_TIMEOUT", -6: "RX_ERR_UNSUPPORTED",
+                -7: "RX_ERR_STATE"}
+
+#: Every symbol include/rx.h declares.
+EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_frame",
+           "rx_attend_suffix", "rx_attend_batch", "rx_ada_gamma", "rx_adarmsnorm",
+           "rx_get_state", "rx_debug_window", "rx_export_window", "rx_check_device_error",
+           "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error")
+
+
+class RxConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("L", "Hq", "Hkv", "D", "P_cap", "N", "F", "S_cap", "tail_cap", "max_req")]
+
+
+class RxRequest(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_priv", ctypes.c_void_p), ("v_priv", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("n_tok", ctypes.c_int), ("n_priv", ctypes.c_int)]
+
+
+_vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_sigs = {
+    "rx_cache_create": (_i, [ctypes.POINTER(RxConfig), ctypes.POINTER(_vp)]),
+    "rx_cache_destroy": (_i, [_vp]),
+    "rx_pin_prefix": (_i, [_vp, _vp, _vp, _i, _vp]),
+    "rx_push_frame": (_i, [_vp, _vp, _vp, ctypes.POINTER(_i), _vp]),
+    "rx_attend_suffix": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, _vp]),
+    "rx_attend_batch": (_i, [_vp, _i, ctypes.POINTER(RxRequest), _i, _vp]),
+    "rx_ada_gamma": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp]),
+    "rx_adarmsnorm": (_i, [_vp, _vp, _i, _i, _f, _vp, _vp]),
+    "rx_get_state": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i),
+                          ctypes.POINTER(ctypes.c_longlong), _vp]),
+    "rx_debug_window": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), _vp]),
+    "rx_export_window": (_i, [_vp, _i, _vp, _vp, _vp]),
+    "rx_check_device_error": (_i, [_vp, ctypes.POINTER(_i), _vp]),
+    "rx_set_attn_splits": (_i, [_vp, _i]),
+    "rx_launch_count": (ctypes.c_longlong, []),
+    "rx_status_str": (ctypes.c_char_p, [_i]),
+    "rx_last_error": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _sigs.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class RxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.rx_last_error().decode(errors="replace")
+        super().__init__("%s failed: %s: %s" % (where, STATUS_NAMES.get(status, status), msg))
+
+
+def _check(status: int, where: str) -> None:
+    if status != RX_OK:
+        raise RxError(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=torch.bfloat16, name: str = "tensor",
+         device: bool = True) -> Optional[int]:
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t.data_ptr()
+
+
+def launch_count() -> int:
+    return int(_lib.rx_launch_count())
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+class Cache:
+    """The partitioned KV store of one stream (rx_cache_t)."""
+
+    def __init__(self, L: int, Hq: int, Hkv: int, D: int, P_cap: int, N: int, F: int,
+                 S_cap: int, tail_cap: int = 0, max_req: int = 0):
+        self.cfg = RxConfig(L, Hq, Hkv, D, P_cap, N, F, S_cap, tail_cap, max_req)
+        h = _vp()
+        _check(_lib.rx_cache_create(ctypes.byref(self.cfg), ctypes.byref(h)), "rx_cache_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            _check(_lib.rx_cache_destroy(self._h), "rx_cache_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def pin_prefix(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        P = k.shape[1]
+        _check(_lib.rx_pin_prefix(self._h, _ptr(k, name="k", device=False),
+                                  _ptr(v, name="v", device=False), P, _stream(stream)),
+               "rx_pin_prefix")
+
+    def push_frame(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> int:
+        ev = _i(0)
+        _check(_lib.rx_push_frame(self._h, _ptr(k, name="k"), _ptr(v, name="v"),
+                                  ctypes.byref(ev), _stream(stream)), "rx_push_frame")
+        return ev.value
+
+    def attend_suffix(self, layer: int, q: torch.Tensor, k_dyn: torch.Tensor, v_dyn: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        S = q.shape[0]
+        if out is None:
+            out = torch.empty_like(q)
+        _check(_lib.rx_attend_suffix(self._h, layer, _ptr(q, name="q"), _ptr(k_dyn, name="k_dyn"),
+                                     _ptr(v_dyn, name="v_dyn"), S, _ptr(out, name="out"),
+                                     _stream(stream)), "rx_attend_suffix")
+        return out
+
+    def attend_batch(self, layer: int, requests: Sequence[Tuple], stream=None) -> List[torch.Tensor]:
+        """requests: (q [n][Hq][D], k_priv [t][Hkv][D] or None, v_priv, out or None)."""
+        arr = (RxRequest * max(1, len(requests)))()
+        outs = []
+        for i, r in enumerate(requests):
+            q, kp, vp = r[0], r[1], r[2]
+            out = r[3] if len(r) > 3 and r[3] is not None else torch.empty_like(q)
+            n_priv = 0 if kp is None else kp.shape[0]
+            arr[i] = RxRequest(_ptr(q, name="q"), _ptr(kp, name="k_priv") if n_priv else None,
+                               _ptr(vp, name="v_priv") if n_priv else None, _ptr(out, name="out"),
+                               q.shape[0], n_priv)
+            outs.append(out)
+        _check(_lib.rx_attend_batch(self._h, layer, arr, len(requests), _stream(stream)),
+               "rx_attend_batch")
+        return outs
+
+    def get_state(self, stream=None) -> Tuple[int, int, int]:
+        h, v, p = _i(0), _i(0), ctypes.c_longlong(0)
+        _check(_lib.rx_get_state(self._h, ctypes.byref(h), ctypes.byref(v), ctypes.byref(p),
+                                 _stream(stream)), "rx_get_state")
+        return h.value, v.value, p.value
+
+    def debug_window(self, stream=None) -> List[int]:
+        slots = (_i * self.cfg.N)()
+        valid = _i(0)
+        _check(_lib.rx_debug_window(self._h, slots, ctypes.byref(valid), _stream(stream)),
+               "rx_debug_window")
+        return [slots[i] for i in range(valid.value)]
+
+    def export_window(self, layer: int, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        valid = len(self.debug_window(stream))
+        c = self.cfg
+        k = torch.empty((valid * c.F, c.Hkv, c.D), dtype=torch.bfloat16, device="cuda")
+        v = torch.empty_like(k)
+        if valid:
+            _check(_lib.rx_export_window(self._h, layer, _ptr(k), _ptr(v), _stream(stream)),
+                   "rx_export_window")
+        return k, v
+
+    def check_device_error(self, stream=None) -> int:
+        code = _i(0)
+        _check(_lib.rx_check_device_error(self._h, ctypes.byref(code), _stream(stream)),
+               "rx_check_device_error")
+        return code.value
+
+    def set_attn_splits(self, splits: int) -> None:
+        _check(_lib.rx_set_attn_splits(self._h, splits), "rx_set_attn_splits")
+
+
+def ada_gamma(t: torch.Tensor, state: torch.Tensor, W1: torch.Tensor, b1: torch.Tensor,
+              W2: torch.Tensor, b2: torch.Tensor, emb_dim: int,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gamma [n_sets][n_cond][d] for weights W1 [n_sets][hidden][cond], W2 [n_sets][d][hidden]."""
+    n_cond = t.shape[0]
+    state_dim = state.shape[1] if state.dim() == 2 else 0
+    n_sets, hidden, cond = W1.shape
+    d = W2.shape[1]
+    if cond != emb_dim + state_dim:
+        raise ValueError("W1 input width %d != emb_dim + state_dim = %d" % (cond, emb_dim + state_dim))
+    if out is None:
+        out = torch.empty((n_sets, n_cond, d), dtype=torch.float32, device=t.device)
+    _check(_lib.rx_ada_gamma(_ptr(t, torch.float32, "t"), _ptr(state, torch.float32, "state"),
+                             n_cond, emb_dim, state_dim, _ptr(W1, name="W1"), _ptr(b1, name="b1"),
+                             hidden, _ptr(W2, name="W2"), _ptr(b2, name="b2"), d, n_sets,
+                             _ptr(out, torch.float32, "gamma"), _stream(stream)), "rx_ada_gamma")
+    return out
+
+
+def adarmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    rows, d = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check(_lib.rx_adarmsnorm(_ptr(x, name="x"), _ptr(gamma, torch.float32, "gamma"), rows, d,
+                              float(eps), _ptr(out, name="y"), _stream(stream)), "rx_adarmsnorm")
+    return out

@@ -1,0 +1,91 @@
+"""The C-ABI library loads and exports every symbol include/rx.h declares; host
+argument validation rejects bad calls before touching a device (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests._util import LIB, ROOT, ensure_built
+
+HEADER = os.path.join(ROOT, "include", "rx.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rx_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        ensure_built()
+    except RuntimeError as e:  # pragma: no cover
+        pytest.skip("cannot build librx.so here: %s" % e)
+    return ctypes.CDLL(LIB)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(lib, n), "librx.so does not export %s" % n
+    from partitioned_kv_cache_gb300 import rx
+    assert sorted(rx.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    lib.rx_status_str.restype = ctypes.c_char_p
+    assert lib.rx_status_str(0) == b"RX_OK"
+    assert lib.rx_status_str(-3) == b"RX_ERR_CAPACITY"
+    assert lib.rx_status_str(-99) == b"RX_ERR_UNKNOWN"
+
+
+def test_create_rejects_bad_configs_without_a_device(lib):
+    from partitioned_kv_cache_gb300 import rx
+    h = ctypes.c_void_p()
+    bad = [
+        rx.RxConfig(0, 8, 1, 256, 64, 8, 256, 51, 0, 0),     # L = 0
+        rx.RxConfig(1, 8, 3, 256, 64, 8, 256, 51, 0, 0),     # Hq % Hkv
+        rx.RxConfig(1, 8, 1, 96, 64, 8, 256, 51, 0, 0),      # D
+        rx.RxConfig(1, 8, 1, 256, 64, 0, 256, 51, 0, 0),     # N = 0
+        rx.RxConfig(1, 8, 1, 256, -1, 8, 256, 51, 0, 0),     # P_cap < 0
+        rx.RxConfig(1, 6, 1, 256, 64, 8, 256, 51, 0, 0),     # G = 6 not a power of two
+    ]
+    for cfg in bad:
+        st = rx._lib.rx_cache_create(ctypes.byref(cfg), ctypes.byref(h))
+        assert st in (-1, -6), st
+        assert h.value is None
+    assert rx._lib.rx_cache_create(None, ctypes.byref(h)) == -1
+
+
+def test_norm_and_gamma_reject_bad_arguments(lib):
+    from partitioned_kv_cache_gb300 import rx
+    L = rx._lib
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    assert L.rx_adarmsnorm(p, p, 4, 7, 1e-6, p + 1024, None) == -1       # d % 8
+    assert L.rx_adarmsnorm(p, p, -1, 8, 1e-6, p + 1024, None) == -1      # rows < 0
+    assert L.rx_adarmsnorm(p, p, 4, 8, 1e-6, p, None) == -1              # alias
+    assert L.rx_adarmsnorm(p + 2, p, 4, 8, 1e-6, p + 1024, None) == -1   # misaligned
+    assert L.rx_adarmsnorm(p, p, 0, 8, 1e-6, p + 1024, None) == 0        # empty: no-op
+    assert L.rx_ada_gamma(p, p, 0, 16, 16, p, p, 64, p, p, 128, 1, p, None) == -1     # n_cond
+    assert L.rx_ada_gamma(p, p, 17, 16, 16, p, p, 64, p, p, 128, 1, p, None) == -1    # n_cond
+    assert L.rx_ada_gamma(p, p, 1, 15, 16, p, p, 64, p, p, 128, 1, p, None) == -1     # odd emb
+    assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 60, p, p, 128, 1, p, None) == -1     # hidden % 8
+    assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 64, p, p, 100, 1, p, None) == -1     # d % 8
+    assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 64, p, p, 128, 0, p, None) == -1     # n_sets
+    L.rx_last_error.restype = ctypes.c_char_p
+    assert b"n_sets" in L.rx_last_error()
+
+
+def test_cache_calls_reject_null_handle(lib):
+    from partitioned_kv_cache_gb300 import rx
+    L = rx._lib
+    assert L.rx_cache_destroy(None) == 0
+    assert L.rx_pin_prefix(None, None, None, 0, None) == -1
+    assert L.rx_push_frame(None, None, None, None, None) == -1
+    assert L.rx_attend_suffix(None, 0, None, None, None, 1, None, None) == -1
+    assert L.rx_attend_batch(None, 0, None, 0, None) == -1
+    assert L.rx_set_attn_splits(None, 0) == -1

@@ -1,0 +1,69 @@
+"""AdaRMSNorm and its gamma MLP on the GPU against the fp64 oracle.
+
+"Reflex: Real-Time VLA Control through Streaming Inference", §III Eq. (2),
+"Model components" (MLP), §V forward (FP32 mean of squares).  Bar: relative
+error <= 1e-2 elementwise and no NaN/Inf for inputs spanning 1e-6..1e3.
+"""
+import numpy as np
+import pytest
+
+from oracle import adarms as OA
+from partitioned_kv_cache_gb300 import workload as W
+from tests._util import check_norm, dev, ensure_built, host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rx():
+    ensure_built()
+    from partitioned_kv_cache_gb300 import rx as m
+    return m
+
+
+@pytest.mark.parametrize("name,n_sets", [("c1", 2), ("c2", 3)])
+def test_gamma_matches_oracle(rx, name, n_sets):
+    import torch
+    wl = W.WORKLOADS[name]
+    seed, tick = 9, 2
+    ws = [W.mlp_weights(wl, seed, i // 2, i % 2) for i in range(n_sets)]
+    W1, b1, W2, b2 = (dev(np.stack([w[j] for w in ws])) for j in range(4))
+    t = torch.from_numpy(W.timesteps(wl)).cuda()
+    st = W.robot_state(wl, seed, tick)
+    state = torch.from_numpy(np.repeat(st[None], wl.steps, axis=0)).cuda()
+    gamma = rx.ada_gamma(t, state, W1, b1, W2, b2, wl.emb_dim).cpu().numpy()
+    for i in range(n_sets):
+        w64 = [W.bf16_bits_to_f64(a) for a in ws[i]]
+        for k, tk in enumerate(W.timesteps(wl)):
+            ref = OA.gamma_mlp(OA.conditioning(float(tk), st, wl.emb_dim), *w64)
+            np.testing.assert_allclose(gamma[i, k], ref, rtol=0, atol=2e-5)
+
+
+@pytest.mark.parametrize("rows,d", [(51, 1024), (8, 128), (3, 4096), (5, 8), (1, 2048), (300, 1000)])
+def test_norm_matches_oracle_across_magnitudes(rx, rows, d):
+    import torch
+    x = W.magnitude_sweep(rows, d, seed=rows * d)
+    gamma = (1.0 + 0.1 * np.random.default_rng(d).standard_normal(d)).astype(np.float32)
+    y = rx.adarmsnorm(dev(x), torch.from_numpy(gamma).cuda(), 1e-6)
+    ref = OA.ada_rms_norm(W.bf16_bits_to_f64(x), gamma.astype(np.float64), 1e-6)
+    check_norm(host64(y), ref)
+
+
+def test_norm_of_suffix_activations_with_mlp_gamma(rx):
+    import torch
+    wl = W.WORKLOADS["c2"]
+    x = W.norm_input(wl, 1, 0, 0, 0, 0)
+    w = W.mlp_weights(wl, 1, 0, 0)
+    st = W.robot_state(wl, 1, 0)
+    g = rx.ada_gamma(torch.tensor([1.0], device="cuda"), torch.from_numpy(st[None]).cuda(),
+                     *(dev(a)[None] for a in w), wl.emb_dim)[0, 0]
+    y = rx.adarmsnorm(dev(x), g, wl.eps)
+    ref_g = OA.gamma_mlp(OA.conditioning(1.0, st, wl.emb_dim), *(W.bf16_bits_to_f64(a) for a in w))
+    check_norm(host64(y), OA.ada_rms_norm(W.bf16_bits_to_f64(x), ref_g, wl.eps))
+
+
+def test_zero_rows_is_a_noop(rx):
+    import torch
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(64, device="cuda")
+    assert rx.adarmsnorm(x, g, 1e-6).shape == (0, 64)

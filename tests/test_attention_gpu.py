@@ -1,0 +1,184 @@
+"""Partitioned attention on the GPU against the fp64 oracle.
+
+"Reflex: Real-Time VLA Control through Streaming Inference", §III Eq. (1) and
+Proposition A.1 / Table 4 (partitioned output equals full-batch attention).
+Tolerance on unit-scale inputs: max-abs 1e-2, mean-abs 1e-3.  Full-size
+workloads are checked on sampled suffix tokens that the oracle computes one by
+one, in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention as OA
+from oracle.pipeline import OracleStream
+from partitioned_kv_cache_gb300 import workload as W
+from tests._util import check_attention, dev, ensure_built, host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rx():
+    ensure_built()
+    from partitioned_kv_cache_gb300 import rx as m
+    return m
+
+
+def _make(rx, wl, seed, P=None):
+    P = wl.P if P is None else P
+    cache = rx.Cache(wl.L, wl.Hq, wl.Hkv, wl.D, max(wl.P, P), wl.N, wl.F, wl.S,
+                     wl.tail_cap, wl.n_lang)
+    pk, pv = W.pinned_kv(wl, seed, P)
+    cache.pin_prefix(dev(pk), dev(pv))
+    return cache
+
+
+def _attend(cache, wl, seed, tick, step, layer, S=None):
+    q, kd, vd = W.suffix_qkv(wl, seed, tick, step, layer, S)
+    return cache.attend_suffix(layer, dev(q), dev(kd), dev(vd))
+
+
+def _oracle_attend(ost, wl, seed, tick, step, layer, S=None, tokens=None):
+    q, kd, vd = (W.bf16_bits_to_f64(a) for a in W.suffix_qkv(wl, seed, tick, step, layer, S))
+    if tokens is not None:
+        q = q[np.asarray(tokens)]
+    ks, vs = ost.regions(layer, kd, vd)
+    return OA.partitioned_attention(q, ks, vs)
+
+
+@pytest.mark.parametrize("name,ticks,steps", [("c1", range(4), (0, 1, 2)),
+                                              ("c2", (0, 1, 3, 4, 5), (0, 9))])
+def test_stream_parity(rx, name, ticks, steps):
+    wl = W.WORKLOADS[name]
+    seed = 1
+    cache = _make(rx, wl, seed)
+    ost = OracleStream(wl, seed)
+    done = -1
+    for tick in ticks:
+        while done < tick:
+            done += 1
+            fk, fv = W.frame_kv(wl, seed, done)
+            cache.push_frame(dev(fk), dev(fv))
+            ost.push(done)
+        for k in steps:
+            for layer in range(wl.L):
+                got = host64(_attend(cache, wl, seed, tick, k, layer))
+                check_attention(got, _oracle_attend(ost, wl, seed, tick, k, layer))
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
+def test_before_any_push_attends_pinned_and_dynamic_only(rx):
+    wl = W.WORKLOADS["c2"]
+    cache = _make(rx, wl, 2)
+    ost = OracleStream(wl, 2)
+    got = host64(_attend(cache, wl, 2, 0, 0, 0))
+    check_attention(got, _oracle_attend(ost, wl, 2, 0, 0, 0))
+    cache.close()
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 0])
+def test_split_count_does_not_change_the_result(rx, splits):
+    wl = W.WORKLOADS["c2"]
+    seed = 3
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(splits)
+    ost = OracleStream(wl, seed)
+    for t in range(4):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    got = host64(_attend(cache, wl, seed, 3, 2, 0))
+    check_attention(got, _oracle_attend(ost, wl, seed, 3, 2, 0))
+    cache.close()
+
+
+@pytest.mark.parametrize("S", [1, 7, 16, 17, 50, 51])
+def test_ragged_suffix_lengths(rx, S):
+    wl = W.WORKLOADS["c2"]
+    seed = 4
+    cache = _make(rx, wl, seed)
+    ost = OracleStream(wl, seed)
+    for t in range(2):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    got = host64(_attend(cache, wl, seed, 1, 0, 0, S))
+    check_attention(got, _oracle_attend(ost, wl, seed, 1, 0, 0, S))
+    cache.close()
+
+
+@pytest.mark.parametrize("shape", [
+    dict(L=2, Hq=8, Hkv=2, D=128, P=40, N=3, F=100, S=20),    # GQA, D = 128, ragged tiles
+    dict(L=1, Hq=4, Hkv=4, D=64, P=0, N=2, F=33, S=9),        # MHA, no pinned prefix
+    dict(L=1, Hq=16, Hkv=1, D=256, P=1, N=1, F=1, S=3),       # one-token frame
+    dict(L=1, Hq=128, Hkv=1, D=64, P=70, N=5, F=64, S=2),     # G = 128: one token per tile
+])
+def test_other_shapes(rx, shape):
+    wl = W.Workload("custom", steps=1, ticks=1, d_model=128, emb_dim=16, state_dim=16,
+                    hidden=64, **shape)
+    seed = 5
+    cache = _make(rx, wl, seed)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+        for layer in range(wl.L):
+            got = host64(_attend(cache, wl, seed, t, 0, layer))
+            check_attention(got, _oracle_attend(ost, wl, seed, t, 0, layer))
+    cache.close()
+
+
+@pytest.mark.parametrize("name", ["c3", "c4"])
+def test_full_size_sampled_tokens(rx, name):
+    """Full workload (18 layers, wrapped window); tokens sampled, all heads."""
+    wl = W.WORKLOADS[name]
+    seed = 6
+    cache = _make(rx, wl, seed)
+    ost = OracleStream(wl, seed)
+    last = wl.N + 2          # the window has wrapped
+    for t in range(last + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    tokens = [0, 1, 25, 49, 50]
+    for layer in (0, 9, wl.L - 1):
+        got = host64(_attend(cache, wl, seed, last, 3, layer))[tokens]
+        ref = _oracle_attend(ost, wl, seed, last, 3, layer, tokens=tokens)
+        # Outlier entries (x20) make the values non-unit-scale: widen by the
+        # output magnitude (bf16 rounding is relative).
+        scale = max(1.0, float(np.abs(ref).max())) if wl.outlier_frac > 0 else 1.0
+        check_attention(got, ref, scale)
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
+def test_repeated_calls_are_deterministic(rx):
+    wl = W.WORKLOADS["c2"]
+    cache = _make(rx, wl, 7)
+    for t in range(5):
+        fk, fv = W.frame_kv(wl, 7, t)
+        cache.push_frame(dev(fk), dev(fv))
+    a = _attend(cache, wl, 7, 4, 0, 0)
+    b = _attend(cache, wl, 7, 4, 0, 0)
+    import torch
+    assert torch.equal(a, b)
+    cache.close()
+
+
+def test_argument_errors(rx):
+    import torch
+    wl = W.WORKLOADS["c1"]
+    cache = _make(rx, wl, 8)
+    q, kd, vd = (dev(a) for a in W.suffix_qkv(wl, 8, 0, 0, 0))
+    with pytest.raises(rx.RxError) as e:
+        cache.attend_suffix(1, q, kd, vd)
+    assert e.value.status == -2
+    big = torch.zeros((wl.S + 1, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rx.RxError) as e:
+        cache.attend_suffix(0, big, big[:, :1].contiguous(), big[:, :1].contiguous())
+    assert e.value.status == -3
+    with pytest.raises(rx.RxError):
+        cache.set_attn_splits(10 ** 6)
+    cache.close()
