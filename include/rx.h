@@ -204,6 +204,39 @@ long long rx_launch_count(void);
 const char* rx_status_str(int status);
 const char* rx_last_error(void);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free attention.  (The pages have no counterpart: this entry
+ * point exists for callers, not for the method.)
+ *
+ * For callers that cannot call cudaMalloc -- a real-time control loop where
+ * an allocation would synchronise the device and stall it, an embedded runtime
+ * that reserved its whole memory budget up front, a plugin inside a framework
+ * that owns the device allocator -- and therefore cannot create an rx_cache.
+ * It computes the same attention as rx_attend_suffix, with the same kernels,
+ * over K/V regions the caller already holds:
+ *   out[s][h] = softmax_j(q[s][h] . K_j / sqrt(D)) V_j over the keys of
+ *   [k_pin (P tokens); k_win (W tokens); k_dyn (n_dyn tokens)].
+ * q, out: bf16 [S][Hq][D]; k_pin/v_pin [P][Hkv][D]; k_win/v_win [W][Hkv][D];
+ * k_dyn/v_dyn [n_dyn][Hkv][D]; all device memory, 16-byte aligned; a region of
+ * 0 tokens may pass NULL.  Nothing is allocated: the kernel's scratch (split
+ * partials and a small state block) lives in one fixed device array of
+ * RX_STATIC_SCRATCH_BYTES that every GPU loading this library holds until
+ * the process exits.  Limit: Hkv * ceil(S*Hq/Hkv / 128) * 128 *
+ * (4*D + 8) bytes must fit in that array (about 8000 query rows at D = 256);
+ * larger calls return RX_ERR_CAPACITY.  The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call shares
+ * the one array and rewrites it, so calls that overlap on the GPU (different
+ * streams, or several host threads) race: serialise them.  A device-side wait
+ * that gives up is recorded in the array and is not reported by this call.
+ * Errors: RX_ERR_ARG, RX_ERR_CAPACITY, RX_ERR_UNSUPPORTED, RX_ERR_CUDA. */
+#define RX_STATIC_SCRATCH_BYTES (8u << 20)
+rx_status rx_attend_regions_static(const void* q, int S, int Hq, int Hkv, int D,
+                                   const void* k_pin, const void* v_pin, int P,
+                                   const void* k_win, const void* v_win, int W,
+                                   const void* k_dyn, const void* v_dyn,
+                                   int n_dyn, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

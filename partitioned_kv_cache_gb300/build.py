@@ -28,7 +28,7 @@ COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE
 # The attention kernel's softmax uses the fast exp2 path; the gamma MLP keeps
 # precise sin/cos/pow/exp.
 PER_FILE = {"partitioned_attn.cu": ["--use_fast_math"]}
-SOURCES = ["rx_api.cu", "ring_append.cu", "adarmsnorm.cu", "partitioned_attn.cu"]
+SOURCES = ["rx_api.cu", "ring_append.cu", "adarmsnorm.cu", "partitioned_attn.cu", "attend_static.cu"]
 
 
 def nvcc() -> str:

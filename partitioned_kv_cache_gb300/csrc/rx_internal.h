@@ -29,6 +29,9 @@ constexpr int kMaxHidden = 2048;      // rx_ada_gamma: hidden width
 // Count of kernel launches made by the library (for benchmark accounting).
 void count_launch(int n = 1);
 
+// Set the message rx_last_error() returns on this thread.
+void set_last_error(const char* where, const char* msg);
+
 // ---- ring append ---------------------------------------------------------
 cudaError_t launch_ring_append(const void* k_src, const void* v_src, void* k_slide,
                                void* v_slide, DevState* st, int L, int N,

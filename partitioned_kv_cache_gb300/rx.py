@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "RX_OK", -1: "RX_ERR_ARG", -2: "RX_ERR_LAYER", -3: "RX_ERR_CA
 EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_frame",
            "rx_attend_suffix", "rx_attend_batch", "rx_ada_gamma", "rx_adarmsnorm",
            "rx_get_state", "rx_debug_window", "rx_export_window", "rx_check_device_error",
-           "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error")
+           "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
+           "rx_attend_regions_static")
 
 
 class RxConfig(ctypes.Structure):
@@ -60,6 +61,8 @@ _sigs = {
     "rx_launch_count": (ctypes.c_longlong, []),
     "rx_status_str": (ctypes.c_char_p, [_i]),
     "rx_last_error": (ctypes.c_char_p, []),
+    "rx_attend_regions_static": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _i,
+                                      _vp, _vp, _i, _vp, _vp]),
 }
 for _name, (_res, _args) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -227,4 +230,29 @@ def adarmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float,
         out = torch.empty_like(x)
     _check(_lib.rx_adarmsnorm(_ptr(x, name="x"), _ptr(gamma, torch.float32, "gamma"), rows, d,
                               float(eps), _ptr(out, name="y"), _stream(stream)), "rx_adarmsnorm")
+    return out
+
+
+def attend_regions_static(q: torch.Tensor, k_pin: Optional[torch.Tensor], v_pin: Optional[torch.Tensor],
+                          k_win: Optional[torch.Tensor], v_win: Optional[torch.Tensor],
+                          k_dyn: Optional[torch.Tensor], v_dyn: Optional[torch.Tensor],
+                          out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Attention over caller-held regions through rx_attend_regions_static.
+
+    For callers that cannot allocate device memory: the library allocates
+    nothing on this path (its scratch is a fixed array inside librx.so), so
+    `out` must be supplied.  Regions are [tokens][Hkv][D] bf16 or None.
+    """
+    S, Hq, D = q.shape
+    regions = [(k_pin, v_pin), (k_win, v_win), (k_dyn, v_dyn)]
+    Hkv = next((k.shape[1] for k, _ in regions if k is not None), 1)
+    counts = [0 if k is None else k.shape[0] for k, _ in regions]
+    ptrs = [(_ptr(k, name="k") if n else None, _ptr(v, name="v") if n else None)
+            for (k, v), n in zip(regions, counts)]
+    _check(_lib.rx_attend_regions_static(_ptr(q, name="q"), S, Hq, Hkv, D,
+                                         ptrs[0][0], ptrs[0][1], counts[0],
+                                         ptrs[1][0], ptrs[1][1], counts[1],
+                                         ptrs[2][0], ptrs[2][1], counts[2],
+                                         _ptr(out, name="out"), _stream(stream)),
+           "rx_attend_regions_static")
     return out
