@@ -153,7 +153,8 @@ rx_status rx_attend_batch(rx_cache_t cache, int layer, const rx_request* reqs,
  * W1: bf16 [n_sets][hidden][emb_dim+state_dim]; b1: bf16 [n_sets][hidden];
  * W2: bf16 [n_sets][d][hidden]; b2: bf16 [n_sets][d];
  * gamma: fp32 [n_sets][n_cond][d] (output).  bf16 weights, fp32 arithmetic.
- * Limits: 1 <= n_cond <= 16, emb_dim even, hidden <= 2048, d % 8 == 0.
+ * Limits: 1 <= n_cond <= 16, emb_dim even, hidden % 16 == 0 and <= 2048,
+ * d % 8 == 0.
  * Errors: RX_ERR_ARG, RX_ERR_CUDA. */
 rx_status rx_ada_gamma(const float* t, const float* state, int n_cond,
                        int emb_dim, int state_dim, const void* W1,

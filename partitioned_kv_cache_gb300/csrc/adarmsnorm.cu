@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) ada_gamma_kernel(
   extern __shared__ float sh[];
   const int cond_dim = emb_dim + state_dim;
   float* c = sh;                        // [n_cond][cond_dim]
-  float* h = sh + n_cond * cond_dim;    // [n_cond][hidden]
+  float* h = sh + ((n_cond * cond_dim + 3) & ~3);   // [n_cond][hidden], 16-byte aligned
   const int set = blockIdx.y;
   const int half = emb_dim / 2;
 
@@ -164,38 +164,40 @@ __global__ void __launch_bounds__(256) ada_gamma_kernel(
   }
   __syncthreads();
 
-  // gamma_k[i] = 1 + W2[i] . h_k + b2[i]: one warp per output row.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // gamma_k[i] = 1 + W2[i] . h_k + b2[i].  Four threads per output row; thread
+  // q of a row takes hidden columns {16t + 4q .. 16t + 4q + 3}, so the four
+  // threads of a row read 64 contiguous bytes of h (shared by the warp's 8
+  // rows: one conflict-free wavefront) and 32 contiguous bytes of W2.
+  const int q = threadIdx.x & 3;
+  const int i = blockIdx.x * kGammaRows + (threadIdx.x >> 2);
   const __nv_bfloat16* W2s = W2 + static_cast<size_t>(set) * d * hidden;
   const __nv_bfloat16* b2s = b2 + static_cast<size_t>(set) * d;
-  const int row_end = min(d, (blockIdx.x + 1) * kGammaRows);
-  const int nvh = hidden >> 3;
-  for (int i = blockIdx.x * kGammaRows + warp; i < row_end; i += 8) {
-    float acc[kMaxCond];
+  float acc[kMaxCond];
 #pragma unroll
-    for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
-    const uint4* wr = reinterpret_cast<const uint4*>(W2s + static_cast<size_t>(i) * hidden);
-    for (int v = lane; v < nvh; v += 32) {
-      float w[8];
-      unpack8(wr[v], w);
-#pragma unroll
-      for (int k = 0; k < kMaxCond; ++k) {
-        if (k < n_cond) {
-          const float* hk = h + k * hidden + 8 * v;
-          float a = acc[k];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) a = fmaf(w[e], hk[e], a);
-          acc[k] = a;
-        }
-      }
-    }
-    const float bias = __bfloat162float(b2s[i]);
+  for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
+  const int ir = i < d ? i : d - 1;   // rows past d compute a duplicate and are not stored
+  const uint2* wr = reinterpret_cast<const uint2*>(W2s + static_cast<size_t>(ir) * hidden);
+  for (int t = 0; t < hidden / 16; ++t) {
+    const int j = 16 * t + 4 * q;
+    const uint2 wv = wr[j >> 2];
+    const float w0 = __uint_as_float(wv.x << 16), w1 = __uint_as_float(wv.x & 0xFFFF0000u);
+    const float w2 = __uint_as_float(wv.y << 16), w3 = __uint_as_float(wv.y & 0xFFFF0000u);
 #pragma unroll
     for (int k = 0; k < kMaxCond; ++k) {
       if (k < n_cond) {
-        const float s = warp_sum(acc[k]);
-        if (lane == 0) gamma[(static_cast<size_t>(set) * n_cond + k) * d + i] = 1.0f + s + bias;
+        const float4 hv = *reinterpret_cast<const float4*>(h + k * hidden + j);
+        acc[k] = fmaf(w0, hv.x, fmaf(w1, hv.y, fmaf(w2, hv.z, fmaf(w3, hv.w, acc[k]))));
       }
+    }
+  }
+  const float bias = __bfloat162float(b2s[ir]);
+#pragma unroll
+  for (int k = 0; k < kMaxCond; ++k) {
+    if (k < n_cond) {
+      float v = acc[k];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (q == 0 && i < d) gamma[(static_cast<size_t>(set) * n_cond + k) * d + i] = 1.0f + v + bias;
     }
   }
 }
@@ -226,7 +228,8 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
                              int state_dim, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
                              int hidden, const __nv_bfloat16* W2, const __nv_bfloat16* b2, int d,
                              int n_sets, float* gamma, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(n_cond) * (emb_dim + state_dim + hidden) * sizeof(float);
+  const size_t c_floats = (static_cast<size_t>(n_cond) * (emb_dim + state_dim) + 3) & ~size_t(3);
+  const size_t smem = (c_floats + static_cast<size_t>(n_cond) * hidden) * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(ada_gamma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -131,7 +131,9 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
       const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
                                 static_cast<uint64_t>(ntok[i]), 1};
       const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2, tok, ntok[i] * tok};
-      const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
+      // K maps (even i) load 64-key boxes, V maps (odd i) the ring's V pieces.
+      const uint32_t rows = (i & 1) ? static_cast<uint32_t>(rx::v_piece_keys(D)) : static_cast<uint32_t>(rx::kBN);
+      const uint32_t box[4] = {64u, 1u, rows, 1u};
       if (!rx::encode_tmap_4d(&tm[i], bases[i], dims, strides, box))
         return reject(RX_ERR_CUDA, "tensor-map encoding failed");
     }

@@ -47,32 +47,38 @@ template <int D>
 struct Layout {
   static constexpr int KB = D / 64;                 // 64-column blocks of the head dim
   static constexpr int Q_BLOCK = kBM * 128;         // one 64-column block of Q: 128 rows x 128 B
-  static constexpr int KV_BLOCK = kBN * 128;        // one 64-column block of a K/V tile
   static constexpr int Q_BYTES = KB * Q_BLOCK;
-  static constexpr int KV_BYTES = KB * KV_BLOCK;
   static constexpr int P_BYTES = kBM * kBN * 2;
+  // K/V stream through a ring of 8 KB pieces.  A K tile is KB pieces (one per
+  // 64-column block: 64 keys x 128 B); a V tile is KB pieces of VK keys each
+  // (all D columns: KB blocks of VK keys x 128 B).  Each piece is released as
+  // soon as the MMAs that read it complete.
+  static constexpr int PIECE = 8192;
+  static constexpr int NS = 16;                     // ring slots
+  static constexpr int VK = v_piece_keys(D);        // keys per V piece
+  static constexpr int PIECES_PER_TILE = 2 * KB;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;     // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_RING = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_RING + NS * PIECE;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int NUM_BARS = 12;
-  static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+  static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;        // slack for 1024-byte alignment
   static constexpr int TMEM_COLS = (D + 2 * kBN) <= 256 ? 256 : 512;
   static_assert(ALLOC <= 232448, "shared memory budget");
+  static_assert(KB * VK * 128 == PIECE, "a V piece fills one ring slot");
 };
 
-// Barrier indices.
-enum : int { B_Q = 0, B_KF = 1, B_VF = 3, B_SF = 5, B_PF = 7, B_PV = 9, B_DRAIN = 11 };
+// Barrier indices: Q, ring full[NS], ring empty[NS], S full[2], P full[2],
+// PV done[2], drain.
+enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39 };
 
 struct AttnParams {
   CUtensorMap tm_q;      // 4-D (D, G, Hkv, S), box (64, G, 1, 128/G)
   CUtensorMap tm_k[3];   // 4-D (D, Hkv, keys, layers), box (64, 1, 64, 1): pin, window, dyn
   CUtensorMap tm_v[3];
   __nv_bfloat16* out;    // [S][Hq][D]
-  float* part_o;         // [Hkv][splits][rows_pad][D]
+  float* part_o;         // [Hkv][splits][D][rows_pad] (column-major per split)
   float2* part_ml;       // [Hkv][splits][rows_pad]
   const DevState* st;
   int* err;
@@ -131,8 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + Lay::OFF_Q;
-  const uint32_t sK = base + Lay::OFF_K;
-  const uint32_t sV = base + Lay::OFF_V;
+  const uint32_t sRing = base + Lay::OFF_RING;
   const uint32_t sP = base + Lay::OFF_P;
   const uint32_t sBar = base + Lay::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lay::OFF_MISC);
@@ -159,9 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q), 1);
+    for (int i = 0; i < Lay::NS; ++i) {
+      mbar_init(BAR(B_FULL + i), 1);
+      mbar_init(BAR(B_EMPTY + i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(B_KF + i), 1);
-      mbar_init(BAR(B_VF + i), 1);
       mbar_init(BAR(B_SF + i), 1);
       mbar_init(BAR(B_PF + i), 128);
       mbar_init(BAR(B_PV + i), 1);
@@ -193,48 +200,61 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   if (n > 0 && warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
+      int issued = 0;   // pieces issued
       mbar_arrive_expect_tx(BAR(B_Q), Lay::Q_BYTES);
       for (int kb = 0; kb < Lay::KB; ++kb)
         tma_load_4d(sQ + kb * Lay::Q_BLOCK, &p.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
-      for (int j = 0; j < n; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(BAR(B_PV + st), ((j - 2) >> 1) & 1, abort_flag)) break;
+      bool ok = true;
+      for (int j = 0; ok && j < n; ++j) {
         const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, p.n_priv);
         const int lay = ti.region == 2 ? 0 : p.layer;
-        mbar_arrive_expect_tx(BAR(B_KF + st), Lay::KV_BYTES);
-        for (int kb = 0; kb < Lay::KB; ++kb)
-          tma_load_4d(sK + st * Lay::KV_BYTES + kb * Lay::KV_BLOCK, &p.tm_k[ti.region], kb * 64,
-                      g, ti.key0, lay, BAR(B_KF + st));
-        mbar_arrive_expect_tx(BAR(B_VF + st), Lay::KV_BYTES);
-        for (int kb = 0; kb < Lay::KB; ++kb)
-          tma_load_4d(sV + st * Lay::KV_BYTES + kb * Lay::KV_BLOCK, &p.tm_v[ti.region], kb * 64,
-                      g, ti.key0, lay, BAR(B_VF + st));
-        issued = j + 1;
+        for (int q = 0; q < Lay::PIECES_PER_TILE; ++q) {
+          const int pc = issued;
+          const int slot = pc % Lay::NS;
+          if (pc >= Lay::NS && !mbar_wait(BAR(B_EMPTY + slot), ((pc / Lay::NS) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sRing + slot * Lay::PIECE;
+          mbar_arrive_expect_tx(BAR(B_FULL + slot), Lay::PIECE);
+          if (q < Lay::KB) {   // K columns [64q, 64q+64) of 64 keys
+            tma_load_4d(dst, &p.tm_k[ti.region], q * 64, g, ti.key0, lay, BAR(B_FULL + slot));
+          } else {             // V keys [VK*vb, VK*vb + VK), all columns
+            const int vb = q - Lay::KB;
+            for (int db = 0; db < Lay::KB; ++db)
+              tma_load_4d(dst + db * Lay::VK * 128, &p.tm_v[ti.region], db * 64, g,
+                          ti.key0 + vb * Lay::VK, lay, BAR(B_FULL + slot));
+          }
+          issued = pc + 1;
+        }
       }
       // Every copy issued must land before the CTA exits, even after an abort.
       volatile int no_abort = 0;
       mbar_wait(BAR(B_Q), 0, &no_abort);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
-        mbar_wait(BAR(B_KF + (j & 1)), (j >> 1) & 1, &no_abort);
-        mbar_wait(BAR(B_VF + (j & 1)), (j >> 1) & 1, &no_abort);
-      }
+      for (int pc = issued - Lay::NS < 0 ? 0 : issued - Lay::NS; pc < issued; ++pc)
+        mbar_wait(BAR(B_FULL + pc % Lay::NS), (pc / Lay::NS) & 1, &no_abort);
     }
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
+      // S_j = Q K_j^T: K piece kb holds columns [64kb, 64kb+64) of the tile's
+      // 64 keys; four K=16 steps per piece.
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait(BAR(B_KF + st), (j >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
+        for (int kb = 0; kb < Lay::KB; ++kb) {
+          const int pc = j * Lay::PIECES_PER_TILE + kb;
+          const int slot = pc % Lay::NS;
+          if (!mbar_wait(BAR(B_FULL + slot), (pc / Lay::NS) & 1, abort_flag)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sQ + kb * Lay::Q_BLOCK + ko, 16, 1024);
-          const uint64_t b = sdesc_sw128(sK + st * Lay::KV_BYTES + kb * Lay::KV_BLOCK + ko, 16, 1024);
-          umma_bf16(tS + st * kBN, a, b, kIdescS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = sdesc_sw128(sQ + kb * Lay::Q_BLOCK + kk * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(sRing + slot * Lay::PIECE + kk * 32, 16, 1024);
+            umma_bf16(tS + st * kBN, a, b, kIdescS, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(BAR(B_EMPTY + slot));
         }
         umma_commit(BAR(B_SF + st));
         return true;
@@ -244,17 +264,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (j + 1 < n && !issue_s(j + 1)) break;
         const int st = j & 1;
         if (!mbar_wait(BAR(B_PF + st), (j >> 1) & 1, abort_flag)) break;
-        if (!mbar_wait(BAR(B_VF + st), (j >> 1) & 1, abort_flag)) break;
-        tc_fence_after();
+        // O += P_j V_j: V piece vb holds keys [VK vb, VK vb + VK) with D along the
+        // 128-byte rows (MN-major): 64-column blocks VK*128 B apart (LBO), 8-key
+        // groups 1024 B apart (SBO).  P (K-major) advances 32 B per 16 keys.
+        for (int vb = 0; ok && vb < Lay::KB; ++vb) {
+          const int pc = j * Lay::PIECES_PER_TILE + Lay::KB + vb;
+          const int slot = pc % Lay::NS;
+          if (!mbar_wait(BAR(B_FULL + slot), (pc / Lay::NS) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // A = P (K-major, 128 x 64 keys); B = V tile, MN-major: D runs along
-          // the 128-byte rows, 64-column blocks Lay::KV_BLOCK apart (LBO),
-          // 8-key groups 1024 B apart (SBO).
-          const uint64_t a = sdesc_sw128(sP + st * Lay::P_BYTES + kk * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sV + st * Lay::KV_BYTES + kk * 16 * 128, Lay::KV_BLOCK, 1024);
-          umma_bf16(tO, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < Lay::VK / 16; ++kk) {
+            const int k16 = vb * (Lay::VK / 16) + kk;   // 16-key step within the tile
+            const uint64_t a = sdesc_sw128(sP + st * Lay::P_BYTES + k16 * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(sRing + slot * Lay::PIECE + kk * 16 * 128, Lay::VK * 128, 1024);
+            umma_bf16(tO, a, b, kIdescO, (j > 0 || k16 > 0) ? 1u : 0u);
+          }
+          umma_commit(BAR(B_EMPTY + slot));
         }
+        if (!ok) break;
         umma_commit(BAR(B_PV + st));
       }
       // No tensor-core work may be in flight when TMEM is released.
@@ -353,16 +383,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           }
         }
       } else {
-        float* dst = p.part_o + part_idx * D;
+        // Partial O is stored column-major per split ([D][rows_pad]): for each
+        // column the 32 lanes of a warp write 32 consecutive rows (128 B).
+        float* dst = p.part_o + (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad * D + R;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float o[32];
           tmem_ld32(tO + c + lane_off, o);
           if (row_valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(c + i) * p.rows_pad] = o[i];
           }
         }
         if (row_valid) p.part_ml[part_idx] = make_float2(m_used, l);
@@ -380,48 +410,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 }
 
 // Combine the splits of every row: m = max m_s, l = sum 2^(m_s - m) l_s,
-// out = sum 2^(m_s - m) O_s / l.  One warp per row, D/32 columns per lane.
+// out = sum 2^(m_s - m) O_s / l.  One warp = 32 consecutive rows x 32
+// columns: lane r owns row r, reads its (m, l) per split (coalesced across
+// lanes) and, per split, 32 columns of the column-major partial (each load a
+// coalesced 128-byte row run), all independent of one another.
 template <int D>
-__global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ part_o,
-                                                         const float2* __restrict__ part_ml,
-                                                         __nv_bfloat16* __restrict__ out,
-                                                         int rows, int rows_pad, int n_splits,
-                                                         int Hq, int G) {
-  constexpr int E = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int R = blockIdx.x * 8 + warp;
-  const int g = blockIdx.y;
-  if (R >= rows) return;
-  const size_t head_base = static_cast<size_t>(g) * n_splits * rows_pad;
+__global__ void __launch_bounds__(32) attn_merge_kernel(const float* __restrict__ part_o,
+                                                        const float2* __restrict__ part_ml,
+                                                        __nv_bfloat16* __restrict__ out,
+                                                        int rows, int rows_pad, int n_splits,
+                                                        int Hq, int G) {
+  const int lane = threadIdx.x;
+  const int R = blockIdx.x * 32 + lane;
+  const int c0 = blockIdx.y * 32;
+  const int g = blockIdx.z;
+  const bool valid = R < rows;
+  const size_t head = static_cast<size_t>(g) * n_splits;
   float M = -INFINITY;
   for (int s = 0; s < n_splits; ++s) {
-    const float2 v = part_ml[head_base + static_cast<size_t>(s) * rows_pad + R];
+    const float2 v = valid ? part_ml[(head + s) * rows_pad + R] : make_float2(-INFINITY, 0.f);
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
-  float acc[E];
+  float acc[32];
 #pragma unroll
-  for (int i = 0; i < E; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
   float lsum = 0.f;
   for (int s = 0; s < n_splits; ++s) {
-    const size_t idx = head_base + static_cast<size_t>(s) * rows_pad + R;
-    const float2 v = part_ml[idx];
-    if (!(v.y > 0.f)) continue;
-    const float w = exp2f(v.x - M);
+    const float2 v = valid ? part_ml[(head + s) * rows_pad + R] : make_float2(-INFINITY, 0.f);
+    const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
     lsum += w * v.y;
-    const float* o = part_o + idx * D + lane * E;
+    if (w != 0.f) {
+      const float* o = part_o + (head + s) * rows_pad * D + static_cast<size_t>(c0) * rows_pad + R;
 #pragma unroll
-    for (int i = 0; i < E; i += 2) {
-      const float2 x = *reinterpret_cast<const float2*>(o + i);
-      acc[i] += w * x.x;
-      acc[i + 1] += w * x.y;
+      for (int i = 0; i < 32; ++i) acc[i] += w * o[static_cast<size_t>(i) * rows_pad];
     }
   }
+  if (!valid) return;
   const float inv = 1.f / lsum;
   const int tok = R / G, h = g * G + R % G;
-  __nv_bfloat16* dst = out + (static_cast<size_t>(tok) * Hq + h) * D + lane * E;
+  uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok) * Hq + h) * D + c0);
 #pragma unroll
-  for (int i = 0; i < E; i += 2)
-    *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+  for (int i = 0; i < 4; ++i)
+    dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv),
+                        pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                        pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                        pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
 }
 
 template <int D>
@@ -439,8 +472,8 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1) return e;
-  dim3 mgrid((prm.rows + 7) / 8, Hkv);
-  attn_merge_kernel<D><<<mgrid, 256, 0, s>>>(prm.part_o, prm.part_ml, prm.out, prm.rows,
+  dim3 mgrid((prm.rows + 31) / 32, D / 32, Hkv);
+  attn_merge_kernel<D><<<mgrid, 32, 0, s>>>(prm.part_o, prm.part_ml, prm.out, prm.rows,
                                               prm.rows_pad, prm.n_splits, prm.Hq, prm.G);
   count_launch();
   return cudaGetLastError();
@@ -476,8 +509,9 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest*
                                    static_cast<uint64_t>(a.Hkv) * a.D * 2,
                                    static_cast<uint64_t>(q.n_priv) * a.Hkv * a.D * 2};
       const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(kBN), 1u};
+      const uint32_t vbox[4] = {64u, 1u, static_cast<uint32_t>(v_piece_keys(a.D)), 1u};
       if (!encode_tmap_4d(&prm.tm_k[2], q.k_priv, dims, strides, box)) return cudaErrorInvalidValue;
-      if (!encode_tmap_4d(&prm.tm_v[2], q.v_priv, dims, strides, box)) return cudaErrorInvalidValue;
+      if (!encode_tmap_4d(&prm.tm_v[2], q.v_priv, dims, strides, vbox)) return cudaErrorInvalidValue;
     } else {
       prm.tm_k[2] = *a.tm_pin_k;   // never read: no dynamic tiles
       prm.tm_v[2] = *a.tm_pin_v;

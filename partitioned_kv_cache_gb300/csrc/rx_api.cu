@@ -217,8 +217,9 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
                               static_cast<uint64_t>(h->pin_rows), static_cast<uint64_t>(c.L)};
     const uint64_t strides[3] = {static_cast<uint64_t>(c.D) * 2, tok, h->pin_rows * tok};
     const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
+    const uint32_t vbox[4] = {64u, 1u, static_cast<uint32_t>(rx::v_piece_keys(c.D)), 1u};
     ok = ok && rx::encode_tmap_4d(&h->tm_pin_k, h->k_pin, dims, strides, box);
-    ok = ok && rx::encode_tmap_4d(&h->tm_pin_v, h->v_pin, dims, strides, box);
+    ok = ok && rx::encode_tmap_4d(&h->tm_pin_v, h->v_pin, dims, strides, vbox);
   }
   {
     const uint64_t wt = static_cast<uint64_t>(c.N) * c.F;
@@ -226,8 +227,9 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
                               static_cast<uint64_t>(c.L)};
     const uint64_t strides[3] = {static_cast<uint64_t>(c.D) * 2, tok, wt * tok};
     const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
+    const uint32_t vbox[4] = {64u, 1u, static_cast<uint32_t>(rx::v_piece_keys(c.D)), 1u};
     ok = ok && rx::encode_tmap_4d(&h->tm_win_k, h->k_win, dims, strides, box);
-    ok = ok && rx::encode_tmap_4d(&h->tm_win_v, h->v_win, dims, strides, box);
+    ok = ok && rx::encode_tmap_4d(&h->tm_win_v, h->v_win, dims, strides, vbox);
   }
   if (!ok) {
     cudaFree(h->mem);
@@ -372,8 +374,8 @@ rx_status rx_ada_gamma(const float* t, const float* state, int n_cond, int emb_d
     return fail(RX_ERR_ARG, "rx_ada_gamma: n_cond = %d not in [1, %d]", n_cond, rx::kMaxCond);
   if (emb_dim < 0 || (emb_dim & 1) || state_dim < 0 || emb_dim + state_dim < 1)
     return fail(RX_ERR_ARG, "rx_ada_gamma: emb_dim must be even, widths >= 0, cond width >= 1");
-  if (hidden < 8 || hidden > rx::kMaxHidden || (hidden & 7))
-    return fail(RX_ERR_ARG, "rx_ada_gamma: hidden = %d must be a multiple of 8 in [8, %d]", hidden, rx::kMaxHidden);
+  if (hidden < 16 || hidden > rx::kMaxHidden || (hidden & 15))
+    return fail(RX_ERR_ARG, "rx_ada_gamma: hidden = %d must be a multiple of 16 in [16, %d]", hidden, rx::kMaxHidden);
   if (d < 8 || (d & 7)) return fail(RX_ERR_ARG, "rx_ada_gamma: d = %d must be a positive multiple of 8", d);
   if (n_sets < 1) return fail(RX_ERR_ARG, "rx_ada_gamma: n_sets < 1");
   if (!t || (state_dim > 0 && !state) || !W1 || !b1 || !W2 || !b2 || !gamma)

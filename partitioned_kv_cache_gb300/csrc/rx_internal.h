@@ -49,6 +49,10 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
 constexpr int kBM = 128;   // query rows per CTA (one tcgen05 M=128 tile)
 constexpr int kBN = 64;    // keys per KV tile
 
+// Keys per V piece of the attention kernel's load ring: one 8 KB piece holds
+// all D columns of this many keys.  The V tensor maps use it as box height.
+__host__ __device__ constexpr int v_piece_keys(int D) { return 16 * (256 / D); }
+
 // One M-tile of queries: `rows` rows starting at row `row0` of a request.
 // Row r of a request is (token r / G, head g*G + r % G).
 struct TileDesc {

@@ -73,7 +73,8 @@ def test_norm_and_gamma_reject_bad_arguments(lib):
     assert L.rx_ada_gamma(p, p, 0, 16, 16, p, p, 64, p, p, 128, 1, p, None) == -1     # n_cond
     assert L.rx_ada_gamma(p, p, 17, 16, 16, p, p, 64, p, p, 128, 1, p, None) == -1    # n_cond
     assert L.rx_ada_gamma(p, p, 1, 15, 16, p, p, 64, p, p, 128, 1, p, None) == -1     # odd emb
-    assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 60, p, p, 128, 1, p, None) == -1     # hidden % 8
+    assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 60, p, p, 128, 1, p, None) == -1     # hidden % 16
+    assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 72, p, p, 128, 1, p, None) == -1     # hidden % 16
     assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 64, p, p, 100, 1, p, None) == -1     # d % 8
     assert L.rx_ada_gamma(p, p, 1, 16, 16, p, p, 64, p, p, 128, 0, p, None) == -1     # n_sets
     L.rx_last_error.restype = ctypes.c_char_p
