@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "rx_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace rx {
 namespace {
@@ -49,6 +50,8 @@ __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict
                                                          const float* __restrict__ gamma,
                                                          int rows, int d, float eps,
                                                          uint4* __restrict__ y) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
@@ -118,6 +121,8 @@ __global__ void __launch_bounds__(256) ada_gamma_kernel(
     int hidden, const __nv_bfloat16* __restrict__ W2, const __nv_bfloat16* __restrict__ b2,
     int d, float* __restrict__ gamma) {
   extern __shared__ float sh[];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int cond_dim = emb_dim + state_dim;
   float* c = sh;                        // [n_cond][cond_dim]
   float* h = sh + ((n_cond * cond_dim + 3) & ~3);   // [n_cond][hidden], 16-byte aligned
@@ -210,17 +215,18 @@ cudaError_t launch_adarmsnorm(const __nv_bfloat16* x, const float* gamma, int ro
   const unsigned int blocks = static_cast<unsigned int>((rows + 7) / 8);
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint4* yv = reinterpret_cast<uint4*>(y);
+  cudaError_t e;
   if (d <= 256)
-    adarmsnorm_kernel<1><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<1>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
   else if (d <= 512)
-    adarmsnorm_kernel<2><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<2>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
   else if (d <= 1024)
-    adarmsnorm_kernel<4><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<4>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
   else if (d <= 2048)
-    adarmsnorm_kernel<8><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<8>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
   else
-    adarmsnorm_kernel<0><<<blocks, 256, 0, s>>>(xv, gamma, rows, d, eps, yv);
-  count_launch();
+    e = launch_k(adarmsnorm_kernel<0>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -236,10 +242,9 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
     if (e != cudaSuccess) return e;
   }
   dim3 grid((d + kGammaRows - 1) / kGammaRows, n_sets);
-  ada_gamma_kernel<<<grid, 256, smem, s>>>(t, state, n_cond, emb_dim, state_dim, W1, b1, hidden,
-                                            W2, b2, d, gamma);
-  count_launch();
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(ada_gamma_kernel, grid, dim3(256), smem, s, t, state, n_cond,
+                                 emb_dim, state_dim, W1, b1, hidden, W2, b2, d, gamma);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rx

@@ -131,13 +131,13 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
       const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
                                 static_cast<uint64_t>(ntok[i]), 1};
       const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2, tok, ntok[i] * tok};
-      // K maps (even i) load 64-key boxes, V maps (odd i) the ring's V pieces.
-      const uint32_t rows = (i & 1) ? static_cast<uint32_t>(rx::v_piece_keys(D)) : static_cast<uint32_t>(rx::kBN);
-      const uint32_t box[4] = {64u, 1u, rows, 1u};
+      const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
       if (!rx::encode_tmap_4d(&tm[i], bases[i], dims, strides, box))
         return reject(RX_ERR_CUDA, "tensor-map encoding failed");
     }
     rx::AttnLaunch a;
+    a.pin_k_tiles = a.pin_v_tiles = a.win_k_tiles = a.win_v_tiles = nullptr;   // caller layout: TMA
+    a.pin_head_stride = a.win_head_stride = 0;
     a.tm_pin_k = &tm[0];
     a.tm_pin_v = &tm[1];
     a.tm_slide_k = &tm[2];

@@ -11,9 +11,13 @@
 //     tile feeds a dense M=128 contraction -- with MQA (Hkv = 1) all 8 heads x
 //     51 tokens share the same keys.
 //   * The key sequence is walked region by region (pinned, window, dynamic) in
-//     64-key tiles loaded by TMA straight from where each region lives; the
-//     window is read in physical slot order, which Proposition A.1 permits.
-//     Keys past a region's length are masked.
+//     64-key tiles read straight from where each region lives; the window is
+//     read in physical slot order, which Proposition A.1 permits.  Keys past a
+//     region's length are masked.  The store keeps its regions pre-tiled in
+//     the operand layout, so a K or V tile is one contiguous bulk copy; the
+//     caller's dynamic K/V (and any untiled region) come in by TMA boxes that
+//     produce the same layout.  K and V tiles stream through a ring of slots;
+//     a K slot is released once Q K^T has read it, a V slot once P V has.
 //   * S = Q K^T and O += P V run on tcgen05 with both accumulators in TMEM
 //     (O: D columns; S: two 64-column buffers).  One thread per row does the
 //     online softmax in the exp2 domain; O is rescaled in TMEM only when the
@@ -23,8 +27,11 @@
 //     fp32 partial (O, m, l); a merge kernel combines them with the global
 //     maximum.  With a single split the CTA writes the bf16 output directly.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
-// MMA issuer, warps 2..5 = softmax and epilogue (TMEM lane quarter = warp % 4).
+// Warp roles (224 threads): warp 0 = copy producer, warp 1 = TMEM allocator and
+// Q K^T issuer, warp 6 = P V issuer, warps 2..5 = softmax and epilogue (TMEM
+// lane quarter = warp % 4).  The two MMA streams are issued by different warps
+// so that queueing Q K^T of the next tile behind the tensor pipe never delays
+// P V of the current one.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,8 +47,9 @@
 namespace rx {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int kTilesPerSplit = 8;            // target key tiles per split
 
 template <int D>
 struct Layout {
@@ -49,24 +57,18 @@ struct Layout {
   static constexpr int Q_BLOCK = kBM * 128;         // one 64-column block of Q: 128 rows x 128 B
   static constexpr int Q_BYTES = KB * Q_BLOCK;
   static constexpr int P_BYTES = kBM * kBN * 2;
-  // K/V stream through a ring of 8 KB pieces.  A K tile is KB pieces (one per
-  // 64-column block: 64 keys x 128 B); a V tile is KB pieces of VK keys each
-  // (all D columns: KB blocks of VK keys x 128 B).  Each piece is released as
-  // soon as the MMAs that read it complete.
-  static constexpr int PIECE = 8192;
-  static constexpr int NS = 16;                     // ring slots
-  static constexpr int VK = v_piece_keys(D);        // keys per V piece
-  static constexpr int PIECES_PER_TILE = 2 * KB;
+  static constexpr int TILE = static_cast<int>(tile_bytes(D));   // one K or V tile: [KB][64][128 B]
+  static constexpr int NS = (128 * 1024) / TILE;    // ring slots (4 at D = 256)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
-  static constexpr int OFF_P = OFF_RING + NS * PIECE;
+  static constexpr int OFF_P = OFF_RING + NS * TILE;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;        // slack for 1024-byte alignment
   static constexpr int TMEM_COLS = (D + 2 * kBN) <= 256 ? 256 : 512;
   static_assert(ALLOC <= 232448, "shared memory budget");
-  static_assert(KB * VK * 128 == PIECE, "a V piece fills one ring slot");
+  static_assert(NS >= 4 && NS <= 16, "ring depth");
 };
 
 // Barrier indices: Q, ring full[NS], ring empty[NS], S full[2], P full[2],
@@ -77,6 +79,9 @@ struct AttnParams {
   CUtensorMap tm_q;      // 4-D (D, G, Hkv, S), box (64, G, 1, 128/G)
   CUtensorMap tm_k[3];   // 4-D (D, Hkv, keys, layers), box (64, 1, 64, 1): pin, window, dyn
   CUtensorMap tm_v[3];
+  const uint8_t* k_tiles[2];   // pre-tiled pin / window of (layer, head 0); null = tensor map
+  const uint8_t* v_tiles[2];
+  long long head_stride[2];    // bytes between heads of a tiled region
   __nv_bfloat16* out;    // [S][Hq][D]
   float* part_o;         // [Hkv][splits][D][rows_pad] (column-major per split)
   float2* part_ml;       // [Hkv][splits][rows_pad]
@@ -122,6 +127,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One contiguous global -> shared copy, completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // All lanes wait on the barrier, then agree: the warp proceeds only if every
 // lane saw the phase complete.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -150,6 +163,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int split = blockIdx.y;
   const int g = blockIdx.z;
 
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_Q), 1);
+    for (int i = 0; i < Lay::NS; ++i) {
+      mbar_init(BAR(B_FULL + i), 1);
+      mbar_init(BAR(B_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_SF + i), 1);
+      mbar_init(BAR(B_PF + i), 128);
+      mbar_init(BAR(B_PV + i), 1);
+    }
+    mbar_init(BAR(B_DRAIN), 2);   // one commit from each MMA issuer
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {   // prefetch only the descriptors this launch uses
+    tma_prefetch_desc(&p.tm_q);
+    for (int r = 0; r < 3; ++r) {
+      if ((r < 2 && p.k_tiles[r]) || (r == 2 && p.n_priv == 0)) continue;
+      tma_prefetch_desc(&p.tm_k[r]);
+      tma_prefetch_desc(&p.tm_v[r]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // Everything above touched only shared memory, TMEM and the parameters; from
+  // here on the kernel reads inputs an earlier kernel may have written.
+  grid_dependency_wait();
+  grid_launch_dependents();
   // Key tiles of this split.  The window length comes from the device-side
   // ring state written by the append kernel earlier in stream order.
   const int valid = *reinterpret_cast<const volatile int*>(&p.st->valid);
@@ -162,35 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int t1 = static_cast<int>(static_cast<long long>(split + 1) * T / p.n_splits);
   const int n = t1 - t0;
 
-  if (threadIdx.x == 0) {
-    mbar_init(BAR(B_Q), 1);
-    for (int i = 0; i < Lay::NS; ++i) {
-      mbar_init(BAR(B_FULL + i), 1);
-      mbar_init(BAR(B_EMPTY + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(B_SF + i), 1);
-      mbar_init(BAR(B_PF + i), 128);
-      mbar_init(BAR(B_PV + i), 1);
-    }
-    mbar_init(BAR(B_DRAIN), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tm_q);
-    for (int r = 0; r < 3; ++r) {
-      tma_prefetch_desc(&p.tm_k[r]);
-      tma_prefetch_desc(&p.tm_v[r]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem;                               // columns [0, D)
   const uint32_t tS = tmem + static_cast<uint32_t>(D);    // two buffers of 64 columns
@@ -199,95 +217,99 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (n > 0 && warp == 0) {
     // ------------------------------------------------------------ producer
+    // Ring order: K_0, V_0, K_1, V_1, ...; item i uses slot i % NS.
     if (lane == 0) {
-      int issued = 0;   // pieces issued
+      int issued = 0;
       mbar_arrive_expect_tx(BAR(B_Q), Lay::Q_BYTES);
       for (int kb = 0; kb < Lay::KB; ++kb)
         tma_load_4d(sQ + kb * Lay::Q_BLOCK, &p.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
-      bool ok = true;
-      for (int j = 0; ok && j < n; ++j) {
+      for (int j = 0; j < n && issued >= 0; ++j) {
         const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, p.n_priv);
         const int lay = ti.region == 2 ? 0 : p.layer;
-        for (int q = 0; q < Lay::PIECES_PER_TILE; ++q) {
-          const int pc = issued;
-          const int slot = pc % Lay::NS;
-          if (pc >= Lay::NS && !mbar_wait(BAR(B_EMPTY + slot), ((pc / Lay::NS) - 1) & 1, abort_flag)) {
-            ok = false;
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = issued;
+          const int slot = it % Lay::NS;
+          if (it >= Lay::NS && !mbar_wait(BAR(B_EMPTY + slot), ((it / Lay::NS) - 1) & 1, abort_flag)) {
+            issued = -issued - 1;   // stop; remember how many were issued
             break;
           }
-          const uint32_t dst = sRing + slot * Lay::PIECE;
-          mbar_arrive_expect_tx(BAR(B_FULL + slot), Lay::PIECE);
-          if (q < Lay::KB) {   // K columns [64q, 64q+64) of 64 keys
-            tma_load_4d(dst, &p.tm_k[ti.region], q * 64, g, ti.key0, lay, BAR(B_FULL + slot));
-          } else {             // V keys [VK*vb, VK*vb + VK), all columns
-            const int vb = q - Lay::KB;
-            for (int db = 0; db < Lay::KB; ++db)
-              tma_load_4d(dst + db * Lay::VK * 128, &p.tm_v[ti.region], db * 64, g,
-                          ti.key0 + vb * Lay::VK, lay, BAR(B_FULL + slot));
+          const uint32_t dst = sRing + slot * Lay::TILE;
+          mbar_arrive_expect_tx(BAR(B_FULL + slot), Lay::TILE);
+          const uint8_t* tiles = ti.region < 2 ? (kv ? p.v_tiles[ti.region] : p.k_tiles[ti.region]) : nullptr;
+          if (tiles) {
+            bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.key0 / kBN) * Lay::TILE,
+                      Lay::TILE, BAR(B_FULL + slot));
+          } else {
+            const CUtensorMap* tm = kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region];
+            for (int kb = 0; kb < Lay::KB; ++kb)
+              tma_load_4d(dst + kb * 8192, tm, kb * 64, g, ti.key0, lay, BAR(B_FULL + slot));
           }
-          issued = pc + 1;
+          issued = it + 1;
         }
       }
+      if (issued < 0) issued = -issued - 1;
       // Every copy issued must land before the CTA exits, even after an abort.
       volatile int no_abort = 0;
       mbar_wait(BAR(B_Q), 0, &no_abort);
-      for (int pc = issued - Lay::NS < 0 ? 0 : issued - Lay::NS; pc < issued; ++pc)
-        mbar_wait(BAR(B_FULL + pc % Lay::NS), (pc / Lay::NS) & 1, &no_abort);
+      for (int it = issued - Lay::NS < 0 ? 0 : issued - Lay::NS; it < issued; ++it)
+        mbar_wait(BAR(B_FULL + it % Lay::NS), (it / Lay::NS) & 1, &no_abort);
     }
   } else if (n > 0 && warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
-      // S_j = Q K_j^T: K piece kb holds columns [64kb, 64kb+64) of the tile's
-      // 64 keys; four K=16 steps per piece.
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        for (int kb = 0; kb < Lay::KB; ++kb) {
-          const int pc = j * Lay::PIECES_PER_TILE + kb;
-          const int slot = pc % Lay::NS;
-          if (!mbar_wait(BAR(B_FULL + slot), (pc / Lay::NS) & 1, abort_flag)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = sdesc_sw128(sQ + kb * Lay::Q_BLOCK + kk * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(sRing + slot * Lay::PIECE + kk * 32, 16, 1024);
-            umma_bf16(tS + st * kBN, a, b, kIdescS, (kb > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(BAR(B_EMPTY + slot));
-        }
-        umma_commit(BAR(B_SF + st));
-        return true;
-      };
-      bool ok = mbar_wait(BAR(B_Q), 0, abort_flag) && issue_s(0);
+      bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
       for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) break;
         const int st = j & 1;
-        if (!mbar_wait(BAR(B_PF + st), (j >> 1) & 1, abort_flag)) break;
-        // O += P_j V_j: V piece vb holds keys [VK vb, VK vb + VK) with D along the
-        // 128-byte rows (MN-major): 64-column blocks VK*128 B apart (LBO), 8-key
-        // groups 1024 B apart (SBO).  P (K-major) advances 32 B per 16 keys.
-        for (int vb = 0; ok && vb < Lay::KB; ++vb) {
-          const int pc = j * Lay::PIECES_PER_TILE + Lay::KB + vb;
-          const int slot = pc % Lay::NS;
-          if (!mbar_wait(BAR(B_FULL + slot), (pc / Lay::NS) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        // S buffer st last held S_{j-2}; the softmax is done with it once it
+        // has published P_{j-2}.
+        if (j >= 2 && !mbar_wait(BAR(B_PF + st), ((j - 2) >> 1) & 1, abort_flag)) break;
+        const int it = 2 * j;
+        const int slot = it % Lay::NS;
+        if (!mbar_wait(BAR(B_FULL + slot), (it / Lay::NS) & 1, abort_flag)) break;
+        tc_fence_after();
+        // S_j = Q K_j^T (both K-major): column block kb of the K tile sits at
+        // kb * 8 KB; four K=16 steps of 32 B within each 128-byte row.
+        const uint32_t kt = sRing + slot * Lay::TILE;
 #pragma unroll
-          for (int kk = 0; kk < Lay::VK / 16; ++kk) {
-            const int k16 = vb * (Lay::VK / 16) + kk;   // 16-key step within the tile
-            const uint64_t a = sdesc_sw128(sP + st * Lay::P_BYTES + k16 * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(sRing + slot * Lay::PIECE + kk * 16 * 128, Lay::VK * 128, 1024);
-            umma_bf16(tO, a, b, kIdescO, (j > 0 || k16 > 0) ? 1u : 0u);
-          }
-          umma_commit(BAR(B_EMPTY + slot));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t kb = kk >> 2, ko = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sQ + kb * Lay::Q_BLOCK + ko, 16, 1024);
+          const uint64_t b = sdesc_sw128(kt + kb * 8192 + ko, 16, 1024);
+          umma_bf16(tS + st * kBN, a, b, kIdescS, kk > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        umma_commit(BAR(B_PV + st));
+        umma_commit(BAR(B_EMPTY + slot));
+        umma_commit(BAR(B_SF + st));
       }
       // No tensor-core work may be in flight when TMEM is released.
+      umma_commit(BAR(B_DRAIN));
+      volatile int no_abort = 0;
+      mbar_wait(BAR(B_DRAIN), 0, &no_abort);
+    }
+  } else if (n > 0 && warp == 6) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
+      for (int j = 0; j < n; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(BAR(B_PF + st), (j >> 1) & 1, abort_flag)) break;
+        const int it = 2 * j + 1;
+        const int slot = it % Lay::NS;
+        if (!mbar_wait(BAR(B_FULL + slot), (it / Lay::NS) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t vt = sRing + slot * Lay::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // A = P (K-major, 128 x 64 keys); B = V tile read MN-major: D runs
+          // along the 128-byte rows, 64-column blocks 8 KB apart (LBO), 8-key
+          // groups 1 KB apart (SBO), 16 keys = 2 KB per K step.
+          const uint64_t a = sdesc_sw128(sP + st * Lay::P_BYTES + kk * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(vt + kk * 16 * 128, 8192, 1024);
+          umma_bf16(tO, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(BAR(B_EMPTY + slot));
+        umma_commit(BAR(B_PV + st));
+      }
       umma_commit(BAR(B_DRAIN));
       volatile int no_abort = 0;
       mbar_wait(BAR(B_DRAIN), 0, &no_abort);
@@ -311,12 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       tmem_ld32(tS + st * kBN + lane_off, s);
       tmem_ld32(tS + st * kBN + 32 + lane_off, s + 32);
       const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, p.n_priv);
-      float mx = -INFINITY;
+      if (ti.nvalid < kBN) {   // ragged tile: keys past the region are not keys
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] = c < ti.nvalid ? s[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < kBN; ++c)
+          if (c >= ti.nvalid) s[c] = -INFINITY;
       }
+      // Row maximum of the raw scores (the scale is positive), as a tree.
+      float t32[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) t32[c] = fmaxf(s[c], s[c + 32]);
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) t32[c] = fmaxf(t32[c], t32[c + w]);
+      const float mx = t32[0] * p.scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + kRescaleThreshold;
       float fac = 1.f;
@@ -338,17 +368,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           tmem_st32(tO + c + lane_off, o);
         }
       }
-      const float mb = m_used == -INFINITY ? 0.f : m_used;
+      // p = 2^(s * scale - m): one FMA feeds each exponential.
+      const float nmb = m_used == -INFINITY ? 0.f : -m_used;
       uint32_t pk[kBN / 2];
-      float rs = 0.f;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBN / 2; ++c) {
-        const float a = exp2f(s[2 * c] - mb);
-        const float b = exp2f(s[2 * c + 1] - mb);
-        rs += a + b;
+        const float a = exp2f(fmaf(s[2 * c], p.scale_log2, nmb));
+        const float b = exp2f(fmaf(s[2 * c + 1], p.scale_log2, nmb));
+        rs[c & 3] += a + b;
         pk[c] = pack_bf16x2(a, b);
       }
-      l += rs;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       // P buffer `st` was last read by P_{j-2} V_{j-2}.
       if (j >= 2 && !warp_wait(BAR(B_PV + st), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
       const uint32_t prow = sP + st * Lay::P_BYTES + row * 128;
@@ -410,42 +441,61 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 }
 
 // Combine the splits of every row: m = max m_s, l = sum 2^(m_s - m) l_s,
-// out = sum 2^(m_s - m) O_s / l.  One warp = 32 consecutive rows x 32
-// columns: lane r owns row r, reads its (m, l) per split (coalesced across
-// lanes) and, per split, 32 columns of the column-major partial (each load a
-// coalesced 128-byte row run), all independent of one another.
+// out = sum 2^(m_s - m) O_s / l.  A block covers 32 consecutive rows x 32
+// columns; lane r owns row r.  The four warps take every fourth split, so up
+// to eight splits' loads are in flight per lane (two per warp, unrolled), each
+// a coalesced 128-byte run of the column-major partial; the warps' sums meet
+// in shared memory.
 template <int D>
-__global__ void __launch_bounds__(32) attn_merge_kernel(const float* __restrict__ part_o,
-                                                        const float2* __restrict__ part_ml,
-                                                        __nv_bfloat16* __restrict__ out,
-                                                        int rows, int rows_pad, int n_splits,
-                                                        int Hq, int G) {
-  const int lane = threadIdx.x;
+__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o,
+                                                         const float2* __restrict__ part_ml,
+                                                         __nv_bfloat16* __restrict__ out,
+                                                         int rows, int rows_pad, int n_splits,
+                                                         int Hq, int G) {
+  __shared__ float red[3][32][33];
+  __shared__ float red_l[3][32];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = blockIdx.x * 32 + lane;
   const int c0 = blockIdx.y * 32;
   const int g = blockIdx.z;
   const bool valid = R < rows;
+  const int Rc = valid ? R : rows - 1;   // keep loads in bounds for padding lanes
   const size_t head = static_cast<size_t>(g) * n_splits;
   float M = -INFINITY;
   for (int s = 0; s < n_splits; ++s) {
-    const float2 v = valid ? part_ml[(head + s) * rows_pad + R] : make_float2(-INFINITY, 0.f);
+    const float2 v = part_ml[(head + s) * rows_pad + Rc];
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
   float acc[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) acc[i] = 0.f;
   float lsum = 0.f;
-  for (int s = 0; s < n_splits; ++s) {
-    const float2 v = valid ? part_ml[(head + s) * rows_pad + R] : make_float2(-INFINITY, 0.f);
-    const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+  const size_t col_off = static_cast<size_t>(c0) * rows_pad + Rc;
+#pragma unroll 2
+  for (int s = warp; s < n_splits; s += 4) {
+    const float2 v = part_ml[(head + s) * rows_pad + Rc];
+    const bool live = v.y > 0.f;
+    const float w = live ? exp2f(v.x - M) : 0.f;
     lsum += w * v.y;
-    if (w != 0.f) {
-      const float* o = part_o + (head + s) * rows_pad * D + static_cast<size_t>(c0) * rows_pad + R;
+    const float* o = part_o + (head + s) * rows_pad * D + col_off;
+    float x[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] += w * o[static_cast<size_t>(i) * rows_pad];
-    }
+    for (int i = 0; i < 32; ++i) x[i] = o[static_cast<size_t>(i) * rows_pad];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] += live ? w * x[i] : 0.f;
   }
-  if (!valid) return;
+  if (warp > 0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) red[warp - 1][i][lane] = acc[i];
+    red_l[warp - 1][lane] = lsum;
+  }
+  __syncthreads();
+  if (warp > 0 || !valid) return;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] += red[0][i][lane] + red[1][i][lane] + red[2][i][lane];
+  lsum += red_l[0][lane] + red_l[1][lane] + red_l[2][lane];
   const float inv = 1.f / lsum;
   const int tok = R / G, h = g * G + R % G;
   uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok) * Hq + h) * D + c0);
@@ -468,15 +518,14 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(m_tiles, prm.n_splits, Hkv);
-  attn_kernel<D><<<grid, kThreads, Lay::ALLOC, s>>>(prm);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(attn_kernel<D>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1) return e;
   dim3 mgrid((prm.rows + 31) / 32, D / 32, Hkv);
-  attn_merge_kernel<D><<<mgrid, 32, 0, s>>>(prm.part_o, prm.part_ml, prm.out, prm.rows,
-                                              prm.rows_pad, prm.n_splits, prm.Hq, prm.G);
-  count_launch();
-  return cudaGetLastError();
+  e = launch_k(attn_merge_kernel<D>, mgrid, dim3(128), 0, s, static_cast<const float*>(prm.part_o),
+               static_cast<const float2*>(prm.part_ml), prm.out, prm.rows, prm.rows_pad, prm.n_splits,
+               prm.Hq, prm.G);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -498,10 +547,14 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest*
       const uint32_t box[4] = {64u, static_cast<uint32_t>(G), 1u, static_cast<uint32_t>(kBM / G)};
       if (!encode_tmap_4d(&prm.tm_q, q.q, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    prm.tm_k[0] = *a.tm_pin_k;
-    prm.tm_v[0] = *a.tm_pin_v;
-    prm.tm_k[1] = *a.tm_slide_k;
-    prm.tm_v[1] = *a.tm_slide_v;
+    if (!a.pin_k_tiles) {
+      prm.tm_k[0] = *a.tm_pin_k;
+      prm.tm_v[0] = *a.tm_pin_v;
+    }
+    if (!a.win_k_tiles) {
+      prm.tm_k[1] = *a.tm_slide_k;
+      prm.tm_v[1] = *a.tm_slide_v;
+    }
     if (q.n_priv > 0) {
       const uint64_t dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hkv),
                                 static_cast<uint64_t>(q.n_priv), 1};
@@ -509,13 +562,15 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest*
                                    static_cast<uint64_t>(a.Hkv) * a.D * 2,
                                    static_cast<uint64_t>(q.n_priv) * a.Hkv * a.D * 2};
       const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(kBN), 1u};
-      const uint32_t vbox[4] = {64u, 1u, static_cast<uint32_t>(v_piece_keys(a.D)), 1u};
       if (!encode_tmap_4d(&prm.tm_k[2], q.k_priv, dims, strides, box)) return cudaErrorInvalidValue;
-      if (!encode_tmap_4d(&prm.tm_v[2], q.v_priv, dims, strides, vbox)) return cudaErrorInvalidValue;
-    } else {
-      prm.tm_k[2] = *a.tm_pin_k;   // never read: no dynamic tiles
-      prm.tm_v[2] = *a.tm_pin_v;
+      if (!encode_tmap_4d(&prm.tm_v[2], q.v_priv, dims, strides, box)) return cudaErrorInvalidValue;
     }
+    prm.k_tiles[0] = static_cast<const uint8_t*>(a.pin_k_tiles);
+    prm.v_tiles[0] = static_cast<const uint8_t*>(a.pin_v_tiles);
+    prm.k_tiles[1] = static_cast<const uint8_t*>(a.win_k_tiles);
+    prm.v_tiles[1] = static_cast<const uint8_t*>(a.win_v_tiles);
+    prm.head_stride[0] = a.pin_head_stride;
+    prm.head_stride[1] = a.win_head_stride;
     prm.out = static_cast<__nv_bfloat16*>(q.out);
     prm.part_o = a.part_o;
     prm.part_ml = a.part_ml;
@@ -531,9 +586,13 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest*
     const int m_tiles = (prm.rows + kBM - 1) / kBM;
     prm.rows_pad = m_tiles * kBM;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
-    // Split the key sequence so that the grid fills the GPU once.
+    // Split the key sequence: about kTilesPerSplit 64-key tiles per CTA (the
+    // per-CTA set-up, Q load and partial write amortise over them), at most
+    // one wave of CTAs.
     const int t_max = (a.P + kBN - 1) / kBN + (a.N * a.F + kBN - 1) / kBN + (q.n_priv + kBN - 1) / kBN;
-    int splits = a.forced_splits > 0 ? a.forced_splits : a.num_sms / (m_tiles * a.Hkv);
+    const int wave = a.num_sms / (m_tiles * a.Hkv);
+    int splits = a.forced_splits > 0 ? a.forced_splits : (t_max + kTilesPerSplit - 1) / kTilesPerSplit;
+    if (a.forced_splits <= 0 && splits > wave) splits = wave;
     splits = splits < 1 ? 1 : splits;
     splits = splits > t_max ? t_max : splits;
     splits = splits > a.max_splits ? a.max_splits : splits;

@@ -1,39 +1,59 @@
 // ring_append.cu -- O(1) FIFO append of one observation frame into every
-// layer's sliding window.
+// layer's sliding window, and the tiled store layout it writes.
 //
 // "Reflex: Real-Time VLA Control through Streaming Inference", §III "System
 // architecture": each tick enqueues the newest frame and evicts the oldest;
 // §V "Key implementation": add_new_prefix() adds the new tokens and reports
 // evictions, evict_source_prefix() drops the oldest frame from all layers.
 //
-// The window of layer l is N frame slots [l][slot][F][Hkv][D].  A push copies
-// the frame into slot `head` of every layer -- overwriting the oldest frame
-// once the window is full, which is the eviction -- and advances
-// head <- (head+1) mod N, valid <- min(valid+1, N).  Nothing else moves.
-// The state update is done on the device by the last CTA to finish, so a
-// captured CUDA graph replays pushes correctly.
+// The window of (layer l, K/V head g) holds N frame slots of F tokens; slot s
+// covers window tokens [s*F, s*F + F).  A push writes the frame into slot
+// `head` of every layer -- overwriting the oldest frame once the window is
+// full, which is the eviction -- and advances head <- (head+1) mod N,
+// valid <- min(valid+1, N).  Nothing else moves.  The state update is done on
+// the device by the last CTA to finish, so a captured CUDA graph replays
+// pushes correctly.
+//
+// Tokens are stored in the tiled layout described in rx_internal.h (tiles of
+// 64 tokens, 128-byte rows, chunk ^ (token & 7) swizzle), so that the
+// attention kernel moves a whole tile with one bulk copy.  The same packing
+// serves the one-time pinned-prefix copy.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "rx_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace rx {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecPerThread = 4;   // 16-byte vectors per thread per tensor
+constexpr int kVecPerThread = 4;   // 16-byte chunks per thread per tensor
 
-__global__ void __launch_bounds__(kThreads) ring_append_kernel(
-    const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint4* __restrict__ k_win,
-    uint4* __restrict__ v_win, DevState* st, int L, int N, long long frame_vecs) {
-  // Every CTA reads head before any CTA can update it (the update waits for
-  // all CTAs to arrive).
-  const int head = *reinterpret_cast<volatile int*>(&st->head);
-  const long long total = static_cast<long long>(L) * frame_vecs;
+// Byte offset of 16-byte chunk c of token tok of (layer l, head g).
+__device__ __forceinline__ long long tiled_offset(int l, int g, int Hkv, int T, int D, int tok,
+                                                  int c) {
+  const int t = tok >> 6, r = tok & 63, kb = c >> 3, cb = c & 7;
+  return ((static_cast<long long>(l) * Hkv + g) * T + t) * tile_bytes(D) + kb * 8192LL + r * 128 +
+         ((cb ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads) pack_tiles_kernel(
+    const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint8_t* __restrict__ k_dst,
+    uint8_t* __restrict__ v_dst, int L, int n, int Hkv, int D, int T, int tok0, DevState* st,
+    int F, int N) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  // A ring append reads head before any CTA can update it (the update waits
+  // for every CTA to arrive).
+  const int head = st ? *reinterpret_cast<volatile int*>(&st->head) : 0;
+  const int base_tok = st ? head * F : tok0;
+  const int cpt = D >> 3;   // 16-byte chunks per token and head
+  const long long total = static_cast<long long>(L) * n * Hkv * cpt;
   const long long stride = static_cast<long long>(gridDim.x) * kThreads;
-  long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
-  for (; i < total; i += stride * kVecPerThread) {
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += stride * kVecPerThread) {
     uint4 kv[kVecPerThread], vv[kVecPerThread];
     long long idx[kVecPerThread];
 #pragma unroll
@@ -47,14 +67,20 @@ __global__ void __launch_bounds__(kThreads) ring_append_kernel(
 #pragma unroll
     for (int u = 0; u < kVecPerThread; ++u) {
       if (idx[u] < total) {
-        const long long l = idx[u] / frame_vecs;
-        const long long off = idx[u] - l * frame_vecs;
-        const long long dst = (l * N + head) * frame_vecs + off;
-        k_win[dst] = kv[u];
-        v_win[dst] = vv[u];
+        long long rest = idx[u];
+        const int c = static_cast<int>(rest % cpt);
+        rest /= cpt;
+        const int g = static_cast<int>(rest % Hkv);
+        rest /= Hkv;
+        const int f = static_cast<int>(rest % n);
+        const int l = static_cast<int>(rest / n);
+        const long long off = tiled_offset(l, g, Hkv, T, D, base_tok + f, c);
+        *reinterpret_cast<uint4*>(k_dst + off) = kv[u];
+        *reinterpret_cast<uint4*>(v_dst + off) = vv[u];
       }
     }
   }
+  if (!st) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -69,23 +95,55 @@ __global__ void __launch_bounds__(kThreads) ring_append_kernel(
   }
 }
 
+__global__ void __launch_bounds__(kThreads) unpack_tiles_kernel(
+    const uint8_t* __restrict__ k_tiles, const uint8_t* __restrict__ v_tiles, uint4* __restrict__ k_dst,
+    uint4* __restrict__ v_dst, int layer, int tok0, int n, int Hkv, int D, int T) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int cpt = D >> 3;
+  const long long total = static_cast<long long>(n) * Hkv * cpt;
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * kThreads) {
+    long long rest = i;
+    const int c = static_cast<int>(rest % cpt);
+    rest /= cpt;
+    const int g = static_cast<int>(rest % Hkv);
+    const int f = static_cast<int>(rest / Hkv);
+    const long long off = tiled_offset(layer, g, Hkv, T, D, tok0 + f, c);
+    k_dst[i] = *reinterpret_cast<const uint4*>(k_tiles + off);
+    v_dst[i] = *reinterpret_cast<const uint4*>(v_tiles + off);
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_ring_append(const void* k_src, const void* v_src, void* k_win, void* v_win,
-                               DevState* st, int L, int N, long long frame_bytes, int num_sms,
-                               cudaStream_t s) {
-  const long long frame_vecs = frame_bytes / 16;
-  const long long total = static_cast<long long>(L) * frame_vecs;
+cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                              int L, int n, int Hkv, int D, int T, int tok0, DevState* st, int F,
+                              int N, int num_sms, cudaStream_t s) {
+  const long long total = static_cast<long long>(L) * n * Hkv * (D >> 3);
   long long blocks = (total + static_cast<long long>(kThreads) * kVecPerThread - 1) /
                      (static_cast<long long>(kThreads) * kVecPerThread);
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  ring_append_kernel<<<static_cast<unsigned int>(blocks), kThreads, 0, s>>>(
-      static_cast<const uint4*>(k_src), static_cast<const uint4*>(v_src),
-      static_cast<uint4*>(k_win), static_cast<uint4*>(v_win), st, L, N, frame_vecs);
-  count_launch();
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(pack_tiles_kernel, dim3(static_cast<unsigned int>(blocks)),
+                                 dim3(kThreads), 0, s, static_cast<const uint4*>(k_src),
+                                 static_cast<const uint4*>(v_src), static_cast<uint8_t*>(k_dst),
+                                 static_cast<uint8_t*>(v_dst), L, n, Hkv, D, T, tok0, st, F, N);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_unpack_tiles(const void* k_tiles, const void* v_tiles, void* k_dst, void* v_dst,
+                                int layer, int tok0, int n, int Hkv, int D, int T, cudaStream_t s) {
+  const long long total = static_cast<long long>(n) * Hkv * (D >> 3);
+  long long blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  const cudaError_t e = launch_k(unpack_tiles_kernel, dim3(static_cast<unsigned int>(blocks)),
+                                 dim3(kThreads), 0, s, static_cast<const uint8_t*>(k_tiles),
+                                 static_cast<const uint8_t*>(v_tiles), static_cast<uint4*>(k_dst),
+                                 static_cast<uint4*>(v_dst), layer, tok0, n, Hkv, D, T);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rx

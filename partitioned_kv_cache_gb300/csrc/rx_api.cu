@@ -3,9 +3,10 @@
 // The store object ("Reflex: Real-Time VLA Control through Streaming
 // Inference", §V "Key implementation": a statically preallocated,
 // zero-initialised ring buffer with a write pointer) owns one device
-// allocation holding, per layer, the pinned region [P_cap][Hkv][D] and the
-// window [N][F][Hkv][D] for K and V, the device-side ring state and the
-// split-KV workspace of the attention kernel.  Every entry point validates its
+// allocation holding, for K and V, the pinned region (P_cap tokens) and the
+// window (N frames x F tokens) of every (layer, head) in the tiled layout of
+// rx_internal.h, the device-side ring state and the split-KV workspace of the
+// attention kernel.  Every entry point validates its
 // arguments on the host, returns an rx_status and never throws.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -15,6 +16,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -53,6 +55,14 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 namespace rx {
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("RX_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 void set_last_error(const char* where, const char* msg) {
   g_last_error = std::string(where) + ": " + msg;
@@ -111,11 +121,11 @@ struct rx_cache {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   int max_splits = 0;
-  int pin_rows = 0;      // allocated pinned rows per layer: max(P_cap, 1)
+  int T_pin = 0;         // tiles of the pinned region per (layer, head), >= 1
+  int T_win = 0;         // tiles of the window per (layer, head)
   int P = 0;             // pinned tokens currently held
   long long host_pushes = 0;
   int forced_splits = 0;
-  CUtensorMap tm_pin_k, tm_pin_v, tm_win_k, tm_win_v;
 };
 
 #define RX_GUARD_BEGIN try {
@@ -177,11 +187,12 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   h->max_splits = h->num_sms < 64 ? h->num_sms : 64;
-  h->pin_rows = c.P_cap > 0 ? c.P_cap : 1;
+  h->T_pin = rx::tiles_for(c.P_cap > 0 ? c.P_cap : 1);
+  h->T_win = rx::tiles_for(static_cast<long long>(c.N) * c.F);
 
-  const size_t tok = static_cast<size_t>(c.Hkv) * c.D * 2;   // bytes per token
-  const size_t pin_b = round_up(static_cast<size_t>(c.L) * h->pin_rows * tok, 256);
-  const size_t win_b = round_up(static_cast<size_t>(c.L) * c.N * c.F * tok, 256);
+  const size_t tile = static_cast<size_t>(rx::tile_bytes(c.D));
+  const size_t pin_b = round_up(static_cast<size_t>(c.L) * c.Hkv * h->T_pin * tile, 256);
+  const size_t win_b = round_up(static_cast<size_t>(c.L) * c.Hkv * h->T_win * tile, 256);
   const int max_tok = c.S_cap > c.tail_cap ? c.S_cap : c.tail_cap;
   const size_t rows_pad = round_up(static_cast<size_t>(max_tok) * G, rx::kBM);
   const size_t part_rows = static_cast<size_t>(c.Hkv) * h->max_splits * rows_pad;
@@ -209,33 +220,6 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   h->dstate = reinterpret_cast<rx::DevState*>(p); p += st_b;
   h->part_o = reinterpret_cast<float*>(p); p += po_b;
   h->part_ml = reinterpret_cast<float2*>(p);
-
-  // Tensor maps of the two cached regions, all layers: (D, Hkv, tokens, L).
-  bool ok = true;
-  {
-    const uint64_t dims[4] = {static_cast<uint64_t>(c.D), static_cast<uint64_t>(c.Hkv),
-                              static_cast<uint64_t>(h->pin_rows), static_cast<uint64_t>(c.L)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(c.D) * 2, tok, h->pin_rows * tok};
-    const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
-    const uint32_t vbox[4] = {64u, 1u, static_cast<uint32_t>(rx::v_piece_keys(c.D)), 1u};
-    ok = ok && rx::encode_tmap_4d(&h->tm_pin_k, h->k_pin, dims, strides, box);
-    ok = ok && rx::encode_tmap_4d(&h->tm_pin_v, h->v_pin, dims, strides, vbox);
-  }
-  {
-    const uint64_t wt = static_cast<uint64_t>(c.N) * c.F;
-    const uint64_t dims[4] = {static_cast<uint64_t>(c.D), static_cast<uint64_t>(c.Hkv), wt,
-                              static_cast<uint64_t>(c.L)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(c.D) * 2, tok, wt * tok};
-    const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(rx::kBN), 1u};
-    const uint32_t vbox[4] = {64u, 1u, static_cast<uint32_t>(rx::v_piece_keys(c.D)), 1u};
-    ok = ok && rx::encode_tmap_4d(&h->tm_win_k, h->k_win, dims, strides, box);
-    ok = ok && rx::encode_tmap_4d(&h->tm_win_v, h->v_win, dims, strides, vbox);
-  }
-  if (!ok) {
-    cudaFree(h->mem);
-    delete h;
-    return fail(RX_ERR_CUDA, "rx_cache_create: tensor-map encoding failed");
-  }
   *out = h;
   return RX_OK;
   RX_GUARD_END
@@ -262,12 +246,35 @@ rx_status rx_pin_prefix(rx_cache_t h, const void* k, const void* v, int P, void*
   if (P > 0 && (!k || !v)) return fail(RX_ERR_ARG, "rx_pin_prefix: null K/V");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (P > 0) {
-    const size_t tok = static_cast<size_t>(c.Hkv) * c.D * 2;
-    const size_t width = static_cast<size_t>(P) * tok;
-    const size_t dpitch = static_cast<size_t>(h->pin_rows) * tok;
-    cudaError_t e = cudaMemcpy2DAsync(h->k_pin, dpitch, k, width, width, c.L, cudaMemcpyDefault, s);
+    // The prefix is packed into the tiled layout on the device.  Host (or
+    // misaligned) sources are staged through a temporary device buffer: a
+    // one-time set-up copy.
+    const size_t bytes = static_cast<size_t>(c.L) * P * c.Hkv * c.D * 2;
+    cudaPointerAttributes ak{}, av{};
+    const bool dev_k = cudaPointerGetAttributes(&ak, k) == cudaSuccess && ak.devicePointer != nullptr &&
+                       ak.type != cudaMemoryTypeHost && aligned16(k);
+    const bool dev_v = cudaPointerGetAttributes(&av, v) == cudaSuccess && av.devicePointer != nullptr &&
+                       av.type != cudaMemoryTypeHost && aligned16(v);
+    cudaGetLastError();   // clear a lookup error for unregistered host memory
+    void* tmp = nullptr;
+    const void* sk = k;
+    const void* sv = v;
+    cudaError_t e = cudaSuccess;
+    if (!dev_k || !dev_v) {
+      e = cudaMalloc(&tmp, 2 * bytes);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(tmp, k, bytes, cudaMemcpyDefault, s);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<char*>(tmp) + bytes, v, bytes, cudaMemcpyDefault, s);
+      sk = tmp;
+      sv = static_cast<char*>(tmp) + bytes;
+    }
     if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(h->v_pin, dpitch, v, width, width, c.L, cudaMemcpyDefault, s);
+      e = rx::launch_pack_tiles(sk, sv, h->k_pin, h->v_pin, c.L, P, c.Hkv, c.D, h->T_pin, 0, nullptr,
+                                0, 0, h->num_sms, s);
+    if (tmp) {
+      const cudaError_t e2 = cudaStreamSynchronize(s);
+      cudaFree(tmp);
+      if (e == cudaSuccess) e = e2;
+    }
     if (e != cudaSuccess) return cuda_fail(e, "rx_pin_prefix: copy");
   }
   h->P = P;
@@ -281,9 +288,9 @@ rx_status rx_push_frame(rx_cache_t h, const void* k, const void* v, int* evicted
   if (!k || !v) return fail(RX_ERR_ARG, "rx_push_frame: null K/V");
   if (!aligned16(k) || !aligned16(v)) return fail(RX_ERR_ARG, "rx_push_frame: K/V not 16-byte aligned");
   const rx_config& c = h->cfg;
-  const long long frame_bytes = static_cast<long long>(c.F) * c.Hkv * c.D * 2;
-  cudaError_t e = rx::launch_ring_append(k, v, h->k_win, h->v_win, h->dstate, c.L, c.N,
-                                         frame_bytes, h->num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = rx::launch_pack_tiles(k, v, h->k_win, h->v_win, c.L, c.F, c.Hkv, c.D, h->T_win, 0,
+                                        h->dstate, c.F, c.N, h->num_sms,
+                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rx_push_frame: launch");
   if (evicted) *evicted = h->host_pushes >= c.N ? 1 : 0;
   h->host_pushes += 1;
@@ -293,10 +300,16 @@ rx_status rx_push_frame(rx_cache_t h, const void* k, const void* v, int* evicted
 
 static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   rx::AttnLaunch a;
-  a.tm_pin_k = &h->tm_pin_k;
-  a.tm_pin_v = &h->tm_pin_v;
-  a.tm_slide_k = &h->tm_win_k;
-  a.tm_slide_v = &h->tm_win_v;
+  a.tm_pin_k = a.tm_pin_v = a.tm_slide_k = a.tm_slide_v = nullptr;   // regions are tiled
+  const long long tile = rx::tile_bytes(h->cfg.D);
+  a.pin_head_stride = h->T_pin * tile;
+  a.win_head_stride = h->T_win * tile;
+  const long long pin_layer = static_cast<long long>(layer) * h->cfg.Hkv * a.pin_head_stride;
+  const long long win_layer = static_cast<long long>(layer) * h->cfg.Hkv * a.win_head_stride;
+  a.pin_k_tiles = reinterpret_cast<const char*>(h->k_pin) + pin_layer;
+  a.pin_v_tiles = reinterpret_cast<const char*>(h->v_pin) + pin_layer;
+  a.win_k_tiles = reinterpret_cast<const char*>(h->k_win) + win_layer;
+  a.win_v_tiles = reinterpret_cast<const char*>(h->v_win) + win_layer;
   a.layer = layer;
   a.P = h->P;
   a.F = h->cfg.F;
@@ -461,13 +474,9 @@ rx_status rx_export_window(rx_cache_t h, int layer, void* k_out, void* v_out, vo
   if (r != RX_OK) return r;
   const size_t fb = static_cast<size_t>(c.F) * c.Hkv * c.D * 2;
   for (int i = 0; i < valid; ++i) {
-    const size_t src = (static_cast<size_t>(layer) * c.N + slots[i]) * fb;
-    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(k_out) + i * fb,
-                                    reinterpret_cast<char*>(h->k_win) + src, fb,
-                                    cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(static_cast<char*>(v_out) + i * fb,
-                          reinterpret_cast<char*>(h->v_win) + src, fb, cudaMemcpyDeviceToDevice, s);
+    cudaError_t e = rx::launch_unpack_tiles(h->k_win, h->v_win, static_cast<char*>(k_out) + i * fb,
+                                            static_cast<char*>(v_out) + i * fb, layer, slots[i] * c.F,
+                                            c.F, c.Hkv, c.D, h->T_win, s);
     if (e != cudaSuccess) return cuda_fail(e, "rx_export_window: copy");
   }
   return RX_OK;

@@ -29,13 +29,58 @@ constexpr int kMaxHidden = 2048;      // rx_ada_gamma: hidden width
 // Count of kernel launches made by the library (for benchmark accounting).
 void count_launch(int n = 1);
 
+// Whether kernels are launched with programmatic stream serialization (the
+// next kernel may start its prologue while the previous one drains).  On by
+// default; RX_PDL=0 in the environment turns it off.
+bool pdl_enabled();
+
+// Launch `k` on `s`, with programmatic stream serialization when enabled.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+  count_launch();
+  return e;
+}
+
 // Set the message rx_last_error() returns on this thread.
 void set_last_error(const char* where, const char* msg);
 
-// ---- ring append ---------------------------------------------------------
-cudaError_t launch_ring_append(const void* k_src, const void* v_src, void* k_slide,
-                               void* v_slide, DevState* st, int L, int N,
-                               long long frame_bytes, int num_sms, cudaStream_t s);
+// ---- tiled store layout -----------------------------------------------------
+// The pinned region and the window of every (layer, K/V head) are stored as
+// tiles of 64 tokens, each tile already in the shared-memory layout the
+// attention kernel's tensor-core operands use: [D/64 column blocks][64 tokens]
+// [128 bytes], the eight 16-byte chunks of a 128-byte row permuted by
+// chunk ^ (token & 7) (the 128-byte swizzle).  A tile is then one contiguous
+// 128*D-byte bulk copy.  Region layout: [L][Hkv][tiles][tile bytes].
+constexpr int kTileTok = 64;
+__host__ __device__ constexpr long long tile_bytes(int D) { return 128LL * D; }
+__host__ __device__ constexpr int tiles_for(long long tokens) {
+  return static_cast<int>((tokens + kTileTok - 1) / kTileTok);
+}
+
+// Pack tokens [tok0, tok0 + n) of one region for all layers and heads from
+// the user layout src [L][n][Hkv][D] into the tiled layout (T tiles per
+// (layer, head)).  When `st` is non-null this is a ring append: tok0 is
+// head * F read on the device, and the last CTA advances {head, valid}.
+cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                              int L, int n, int Hkv, int D, int T, int tok0, DevState* st,
+                              int F, int N, int num_sms, cudaStream_t s);
+
+// Inverse of the packing for one layer and token range (test aid):
+// dst [n][Hkv][D] <- tiles.
+cudaError_t launch_unpack_tiles(const void* k_tiles, const void* v_tiles, void* k_dst, void* v_dst,
+                                int layer, int tok0, int n, int Hkv, int D, int T, cudaStream_t s);
 
 // ---- AdaRMSNorm ------------------------------------------------------------
 cudaError_t launch_adarmsnorm(const __nv_bfloat16* x, const float* gamma, int rows, int d,
@@ -49,10 +94,6 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
 constexpr int kBM = 128;   // query rows per CTA (one tcgen05 M=128 tile)
 constexpr int kBN = 64;    // keys per KV tile
 
-// Keys per V piece of the attention kernel's load ring: one 8 KB piece holds
-// all D columns of this many keys.  The V tensor maps use it as box height.
-__host__ __device__ constexpr int v_piece_keys(int D) { return 16 * (256 / D); }
-
 // One M-tile of queries: `rows` rows starting at row `row0` of a request.
 // Row r of a request is (token r / G, head g*G + r % G).
 struct TileDesc {
@@ -63,15 +104,22 @@ struct TileDesc {
 constexpr int kMaxReq = 40;   // requests per batched launch (tensor maps in params)
 
 struct AttnLaunch {
-  // Shared regions (pinned, window) of one layer.
+  // Shared regions (pinned, window) of one layer.  Each is either pre-tiled
+  // (pointers below non-null: bulk copies) or read through its tensor map.
   const CUtensorMap* tm_pin_k;
   const CUtensorMap* tm_pin_v;
   const CUtensorMap* tm_slide_k;
   const CUtensorMap* tm_slide_v;
+  const void* pin_k_tiles;      // tiles of (layer, head 0); nullptr = tensor map
+  const void* pin_v_tiles;
+  const void* win_k_tiles;
+  const void* win_v_tiles;
+  long long pin_head_stride;    // bytes between K/V heads of the tiled regions
+  long long win_head_stride;
   int layer, P, F, N, D, Hq, Hkv;
   const DevState* st;
   int* err;
-  float* part_o;      // workspace: [Hkv][splits][tiles*128][D] fp32
+  float* part_o;      // workspace: [Hkv][splits][D][tiles*128] fp32
   float2* part_ml;    // workspace: [Hkv][splits][tiles*128]
   int max_splits;     // capacity of the workspace in splits
   int forced_splits;  // 0 = automatic

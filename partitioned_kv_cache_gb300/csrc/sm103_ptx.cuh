@@ -24,6 +24,22 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- launch chaining
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor drains.  It must call
+// grid_dependency_wait() before touching any global memory the predecessor
+// (or anything before it in the stream) may have written; the wait returns
+// once the predecessor grid has completed and its writes are visible.  With a
+// plain launch it returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel in the stream be scheduled now (it still waits for this
+// grid to complete before reading its results).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

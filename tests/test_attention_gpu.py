@@ -126,7 +126,14 @@ def test_other_shapes(rx, shape):
         ost.push(t)
         for layer in range(wl.L):
             got = host64(_attend(cache, wl, seed, t, 0, layer))
-            check_attention(got, _oracle_attend(ost, wl, seed, t, 0, layer))
+            ref = _oracle_attend(ost, wl, seed, t, 0, layer)
+            # With only a handful of keys an output is not a unit-scale average:
+            # the kernel's two bf16 roundings (P for the tensor-core product and
+            # the output) are each within 2^-9 of sum_j alpha_j |v_j|, so the
+            # bound is 2^-8 * max|V| when that exceeds the unit-scale 1e-2.
+            _, vs = ost.regions(layer, *(W.bf16_bits_to_f64(a) for a in W.suffix_qkv(wl, seed, t, 0, layer)[1:]))
+            vmax = max(float(np.abs(v).max()) for v in vs if v.size)
+            check_attention(got, ref, max(1.0, 2.0 ** -8 * vmax / 1e-2))
     cache.close()
 
 
