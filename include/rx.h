@@ -22,7 +22,8 @@
  *
  * "OxyGen: Unified KV Cache Management for Vision-Language-Action Models under
  * Multi-Task Parallelism", §"Core method": several requests read one
- * read-only prefill cache while each keeps its own appended KV (rx_attend_batch).
+ * read-only prefill cache while each keeps its own appended KV
+ * (rx_attend_batch).
  *
  * Conventions
  * -----------
@@ -76,8 +77,8 @@ typedef struct rx_config {
   int N;        /* frames in the sliding window (>= 1)                      */
   int F;        /* tokens per frame (>= 1)                                  */
   int S_cap;    /* most query tokens of one attention call (>= 1)           */
-  int tail_cap; /* most private keys of one batched request (>= 0)          */
-  int max_req;  /* most requests of one rx_attend_batch call (>= 0)         */
+  int tail_cap; /* private tail capacity of a language stream (>= 0)        */
+  int max_req;  /* most language query tokens (B*T) of one rx_attend_batch  */
 } rx_config;
 
 /* Allocate and zero every region ("Reflex ...", §V: the ring buffer is
@@ -123,26 +124,38 @@ rx_status rx_attend_suffix(rx_cache_t cache, int layer, const void* q,
                            const void* k_dyn, const void* v_dyn, int S,
                            void* out, void* stream);
 
-/* One request of a batched shared-cache call. */
-typedef struct rx_request {
-  const void* q;      /* bf16 [n_tok][Hq][D]                                 */
-  const void* k_priv; /* bf16 [n_priv][Hkv][D], this request's own keys      */
-  const void* v_priv; /* bf16 [n_priv][Hkv][D]                               */
-  void* out;          /* bf16 [n_tok][Hq][D]                                 */
-  int n_tok;          /* query tokens, >= 1                                  */
-  int n_priv;         /* private keys, >= 0                                  */
-} rx_request;
+/* A dense batch of language streams sharing the cache: B streams of T query
+ * tokens each, every stream with its own appended keys (its private tail). */
+typedef struct rx_stream_batch {
+  const void* q;        /* bf16 [B][T][Hq][D]                                   */
+  const void* k_tail;   /* bf16 [B][tail_cap][Hkv][D]: stream b's appended keys */
+  const void* v_tail;   /* bf16 [B][tail_cap][Hkv][D]                           */
+  const int* tail_len;  /* DEVICE int32 [B]: keys held by each tail, clamped to
+                           [0, tail_cap] by the kernel (read on the device, so a
+                           captured graph follows tails that grow)             */
+  void* out;            /* bf16 [B][T][Hq][D]                                   */
+  int B;                /* streams, >= 0                                        */
+  int T;                /* query tokens per stream, >= 1                        */
+} rx_stream_batch;
 
-/* Shared-cache multi-request attention in one launch ("OxyGen ...",
- * §"Core method", cross-task KV sharing): every request attends over the
- * layer's read-only [pinned; window] plus only its own private keys (the
- * action suffix's k_dyn, or a language stream's appended tail).  Nothing one
- * request supplies enters another's softmax.  reqs: HOST array of nreq
- * entries whose pointers are device memory.  Limits: sum over requests of
- * n_tok <= S_cap + max_req, each n_priv <= max(S_cap, tail_cap),
- * nreq <= max_req + 1.  Errors as rx_attend_suffix. */
-rx_status rx_attend_batch(rx_cache_t cache, int layer, const rx_request* reqs,
-                          int nreq, void* stream);
+/* Shared-cache multi-request attention in ONE launch ("OxyGen ...",
+ * §"Core method": one read-only prefill cache serves the action expert across
+ * its denoising steps while language streams, stacked along a batch
+ * dimension, each append their own KV).  The action suffix attends over
+ * [pinned; window; its k_dyn] exactly as rx_attend_suffix; stream b attends
+ * over [pinned; window; its first tail_len[b] tail keys] and nothing another
+ * stream appended.  Both groups share every K/V tile of the cache in the same
+ * launch.
+ * Action: q_act [S][Hq][D], k_dyn/v_dyn [S][Hkv][D], out_act [S][Hq][D];
+ * S = 0 (pointers may be NULL) for no action suffix; S <= S_cap.
+ * lang: may be NULL (or B = 0) for no language streams; B*T <= max_req and
+ * the cache's tail_cap >= 1.  A stream whose tail is empty and whose cache
+ * regions hold no key gets zeros.
+ * Errors: RX_ERR_ARG, RX_ERR_LAYER, RX_ERR_CAPACITY, RX_ERR_CUDA. */
+rx_status rx_attend_batch(rx_cache_t cache, int layer, const void* q_act,
+                          const void* k_dyn, const void* v_dyn, int S,
+                          void* out_act, const rx_stream_batch* lang,
+                          void* stream);
 
 /* Gamma of AdaRMSNorm ("Reflex ...", §III Eq. 2 and "Model components"):
  * for every weight set i and conditioning vector k

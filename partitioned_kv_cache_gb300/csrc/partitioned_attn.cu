@@ -75,24 +75,37 @@ struct Layout {
 // PV done[2], drain.
 enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39 };
 
+// One group of query rows: the action suffix, or a dense batch of language
+// streams.  Its M-tiles occupy workspace rows [row_base, row_base + m_tiles*128).
+struct SegParams {
+  CUtensorMap tm_q;      // 4-D (D, G, Hkv, tokens), box (64, G, 1, 128/G)
+  CUtensorMap tm_kp;     // private keys: 4-D (D, Hkv, n_priv, 1), box (64, 1, 64, 1)
+  CUtensorMap tm_vp;
+  __nv_bfloat16* out;    // [tokens][Hq][D]
+  const int* tail_len;   // stream mask: keys held by each stream's tail (device)
+  int n_priv;            // private keys
+  int rows;              // tokens * G
+  int row_base;
+  int m_tiles;
+  int tok_per_stream;    // stream mask: query tokens per stream
+  int tail_cap;          // stream mask: private keys per stream; 0 = no mask
+};
+
 struct AttnParams {
-  CUtensorMap tm_q;      // 4-D (D, G, Hkv, S), box (64, G, 1, 128/G)
-  CUtensorMap tm_k[3];   // 4-D (D, Hkv, keys, layers), box (64, 1, 64, 1): pin, window, dyn
-  CUtensorMap tm_v[3];
+  SegParams seg[2];
+  CUtensorMap tm_k[2];   // pin, window when not pre-tiled: (D, Hkv, keys, layers), box (64, 1, 64, 1)
+  CUtensorMap tm_v[2];
   const uint8_t* k_tiles[2];   // pre-tiled pin / window of (layer, head 0); null = tensor map
   const uint8_t* v_tiles[2];
   long long head_stride[2];    // bytes between heads of a tiled region
-  __nv_bfloat16* out;    // [S][Hq][D]
   float* part_o;         // [Hkv][splits][D][rows_pad] (column-major per split)
   float2* part_ml;       // [Hkv][splits][rows_pad]
   const DevState* st;
   int* err;
   int layer;
   int P, F;
-  int n_priv;            // dynamic keys
   int Hq, G;
-  int rows;              // S * G
-  int rows_pad;
+  int rows_pad;          // workspace rows of all segments
   int n_splits;
   float scale_log2;      // log2(e) / sqrt(D)
 };
@@ -159,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int mt = blockIdx.x;
+  const int si = static_cast<int>(blockIdx.x) < p.seg[0].m_tiles ? 0 : 1;
+  const SegParams& sg = p.seg[si];
+  const int mt = blockIdx.x - (si ? p.seg[0].m_tiles : 0);   // M-tile within the segment
   const int split = blockIdx.y;
   const int g = blockIdx.z;
 
@@ -182,12 +197,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     tmem_alloc(smem_u32(tmem_slot), Lay::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {   // prefetch only the descriptors this launch uses
-    tma_prefetch_desc(&p.tm_q);
-    for (int r = 0; r < 3; ++r) {
-      if ((r < 2 && p.k_tiles[r]) || (r == 2 && p.n_priv == 0)) continue;
+  if (warp == 0 && lane == 0) {   // prefetch only the descriptors this CTA uses
+    tma_prefetch_desc(&sg.tm_q);
+    for (int r = 0; r < 2; ++r) {
+      if (p.k_tiles[r]) continue;
       tma_prefetch_desc(&p.tm_k[r]);
       tma_prefetch_desc(&p.tm_v[r]);
+    }
+    if (sg.n_priv > 0) {
+      tma_prefetch_desc(&sg.tm_kp);
+      tma_prefetch_desc(&sg.tm_vp);
     }
   }
   tc_fence_before();
@@ -203,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int win_len = valid * p.F;
   const int nt_pin = (p.P + kBN - 1) / kBN;
   const int nt_win = (win_len + kBN - 1) / kBN;
-  const int nt_dyn = (p.n_priv + kBN - 1) / kBN;
+  const int nt_dyn = (sg.n_priv + kBN - 1) / kBN;
   const int T = nt_pin + nt_win + nt_dyn;
   const int t0 = static_cast<int>(static_cast<long long>(split) * T / p.n_splits);
   const int t1 = static_cast<int>(static_cast<long long>(split + 1) * T / p.n_splits);
@@ -222,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       int issued = 0;
       mbar_arrive_expect_tx(BAR(B_Q), Lay::Q_BYTES);
       for (int kb = 0; kb < Lay::KB; ++kb)
-        tma_load_4d(sQ + kb * Lay::Q_BLOCK, &p.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
+        tma_load_4d(sQ + kb * Lay::Q_BLOCK, &sg.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
       for (int j = 0; j < n && issued >= 0; ++j) {
-        const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, p.n_priv);
+        const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv);
         const int lay = ti.region == 2 ? 0 : p.layer;
         for (int kv = 0; kv < 2; ++kv) {
           const int it = issued;
@@ -240,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.key0 / kBN) * Lay::TILE,
                       Lay::TILE, BAR(B_FULL + slot));
           } else {
-            const CUtensorMap* tm = kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region];
+            const CUtensorMap* tm = ti.region == 2 ? (kv ? &sg.tm_vp : &sg.tm_kp)
+                                                   : (kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region]);
             for (int kb = 0; kb < Lay::KB; ++kb)
               tma_load_4d(dst + kb * 8192, tm, kb * 64, g, ti.key0, lay, BAR(B_FULL + slot));
           }
@@ -319,9 +339,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int R = mt * kBM + row;                      // row within this K/V head
-    const bool row_valid = R < p.rows;
+    const int Rs = mt * kBM + row;                     // row within the segment
+    const bool row_valid = Rs < sg.rows;
+    const int R = sg.row_base + Rs;                    // row within the workspace
     const size_t part_idx = (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad + R;
+    // Stream mask: this row's stream sees private keys [lo, hi) only.
+    int lo = 0, hi = sg.n_priv;
+    if (sg.tail_cap > 0) {
+      lo = hi = 0;
+      if (row_valid) {
+        const int b = (Rs / p.G) / sg.tok_per_stream;
+        lo = b * sg.tail_cap;
+        hi = lo + min(max(sg.tail_len[b], 0), sg.tail_cap);
+      }
+    }
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = n > 0;
@@ -332,8 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       float s[kBN];
       tmem_ld32(tS + st * kBN + lane_off, s);
       tmem_ld32(tS + st * kBN + 32 + lane_off, s + 32);
-      const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, p.n_priv);
-      if (ti.nvalid < kBN) {   // ragged tile: keys past the region are not keys
+      const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv);
+      if (ti.region == 2 && sg.tail_cap > 0) {   // private keys of other streams are not keys
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const int key = ti.key0 + c;
+          if (c >= ti.nvalid || key < lo || key >= hi) s[c] = -INFINITY;
+        }
+      } else if (ti.nvalid < kBN) {   // ragged tile: keys past the region are not keys
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
           if (c >= ti.nvalid) s[c] = -INFINITY;
@@ -395,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (ok) {
       tc_fence_after();
       if (p.n_splits == 1) {
-        const int tok = R / p.G;
-        const int h = g * p.G + R % p.G;
-        __nv_bfloat16* dst = p.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
-        const float inv = 1.f / l;
+        const int tok = Rs / p.G;
+        const int h = g * p.G + Rs % p.G;
+        __nv_bfloat16* dst = sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
+        const float inv = l > 0.f ? 1.f / l : 0.f;   // a row with no key at all gets zeros
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float o[32];
@@ -441,27 +478,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 }
 
 // Combine the splits of every row: m = max m_s, l = sum 2^(m_s - m) l_s,
-// out = sum 2^(m_s - m) O_s / l.  A block covers 32 consecutive rows x 32
-// columns; lane r owns row r.  The four warps take every fourth split, so up
+// out = sum 2^(m_s - m) O_s / l.  A block covers 32 consecutive workspace rows
+// (of one segment) x 32 columns; lane r owns row r.  The four warps take every fourth split, so up
 // to eight splits' loads are in flight per lane (two per warp, unrolled), each
 // a coalesced 128-byte run of the column-major partial; the warps' sums meet
 // in shared memory.
 template <int D>
 __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o,
                                                          const float2* __restrict__ part_ml,
-                                                         __nv_bfloat16* __restrict__ out,
-                                                         int rows, int rows_pad, int n_splits,
+                                                         __nv_bfloat16* out0, int rows0,
+                                                         __nv_bfloat16* out1, int rows1,
+                                                         int row_base1, int rows_pad, int n_splits,
                                                          int Hq, int G) {
   __shared__ float red[3][32][33];
   __shared__ float red_l[3][32];
   grid_dependency_wait();
   grid_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int R = blockIdx.x * 32 + lane;
+  const int R = blockIdx.x * 32 + lane;               // workspace row
+  const int si = static_cast<int>(blockIdx.x) * 32 < row_base1 ? 0 : 1;   // blocks never straddle
+  const int base = si ? row_base1 : 0;
+  const int rows = si ? rows1 : rows0;
+  __nv_bfloat16* out = si ? out1 : out0;
+  if (static_cast<int>(blockIdx.x) * 32 - base >= rows) return;   // padding only
+  const int Rs = R - base;
   const int c0 = blockIdx.y * 32;
   const int g = blockIdx.z;
-  const bool valid = R < rows;
-  const int Rc = valid ? R : rows - 1;   // keep loads in bounds for padding lanes
+  const bool valid = Rs < rows;
+  const int Rc = valid ? R : base + rows - 1;   // keep loads on written rows
   const size_t head = static_cast<size_t>(g) * n_splits;
   float M = -INFINITY;
   for (int s = 0; s < n_splits; ++s) {
@@ -496,8 +540,8 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 #pragma unroll
   for (int i = 0; i < 32; ++i) acc[i] += red[0][i][lane] + red[1][i][lane] + red[2][i][lane];
   lsum += red_l[0][lane] + red_l[1][lane] + red_l[2][lane];
-  const float inv = 1.f / lsum;
-  const int tok = R / G, h = g * G + R % G;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;   // a row with no key at all gets zeros
+  const int tok = Rs / G, h = g * G + Rs % G;
   uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok) * Hq + h) * D + c0);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -521,40 +565,34 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   cudaError_t e = launch_k(attn_kernel<D>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1) return e;
-  dim3 mgrid((prm.rows + 31) / 32, D / 32, Hkv);
+  dim3 mgrid(prm.rows_pad / 32, D / 32, Hkv);
   e = launch_k(attn_merge_kernel<D>, mgrid, dim3(128), 0, s, static_cast<const float*>(prm.part_o),
-               static_cast<const float2*>(prm.part_ml), prm.out, prm.rows, prm.rows_pad, prm.n_splits,
+               static_cast<const float2*>(prm.part_ml), prm.seg[0].out, prm.seg[0].rows,
+               prm.seg[1].out, prm.seg[1].rows, prm.seg[1].row_base, prm.rows_pad, prm.n_splits,
                prm.Hq, prm.G);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest* reqs, int nreq,
+cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment* segs, int nseg,
                                          cudaStream_t s, int* used_splits) {
+  if (nseg < 1 || nseg > 2) return cudaErrorInvalidValue;
   const int G = a.Hq / a.Hkv;
-  for (int r = 0; r < nreq; ++r) {
-    const AttnRequest& q = reqs[r];
-    AttnParams prm;
-    memset(&prm, 0, sizeof(prm));
-    // Q: (D, G, Hkv, S) so that one box of (64, G, 1, 128/G) is a 128-row tile.
-    {
-      const uint64_t dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(G),
-                                static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(q.n_tok)};
-      const uint64_t strides[3] = {static_cast<uint64_t>(a.D) * 2,
-                                   static_cast<uint64_t>(G) * a.D * 2,
-                                   static_cast<uint64_t>(a.Hq) * a.D * 2};
-      const uint32_t box[4] = {64u, static_cast<uint32_t>(G), 1u, static_cast<uint32_t>(kBM / G)};
-      if (!encode_tmap_4d(&prm.tm_q, q.q, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    if (!a.pin_k_tiles) {
-      prm.tm_k[0] = *a.tm_pin_k;
-      prm.tm_v[0] = *a.tm_pin_v;
-    }
-    if (!a.win_k_tiles) {
-      prm.tm_k[1] = *a.tm_slide_k;
-      prm.tm_v[1] = *a.tm_slide_v;
-    }
+  AttnParams prm;
+  memset(&prm, 0, sizeof(prm));
+  int m_total = 0, t_max = 0;
+  const int t_shared = (a.P + kBN - 1) / kBN + (a.N * a.F + kBN - 1) / kBN;
+  for (int i = 0; i < nseg; ++i) {
+    const AttnSegment& q = segs[i];
+    SegParams& sp = prm.seg[i];
+    // Q: (D, G, Hkv, tokens) so that one box of (64, G, 1, 128/G) is a 128-row tile.
+    const uint64_t qdims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(G),
+                               static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(q.tokens)};
+    const uint64_t qstrides[3] = {static_cast<uint64_t>(a.D) * 2, static_cast<uint64_t>(G) * a.D * 2,
+                                  static_cast<uint64_t>(a.Hq) * a.D * 2};
+    const uint32_t qbox[4] = {64u, static_cast<uint32_t>(G), 1u, static_cast<uint32_t>(kBM / G)};
+    if (!encode_tmap_4d(&sp.tm_q, q.q, qdims, qstrides, qbox)) return cudaErrorInvalidValue;
     if (q.n_priv > 0) {
       const uint64_t dims[4] = {static_cast<uint64_t>(a.D), static_cast<uint64_t>(a.Hkv),
                                 static_cast<uint64_t>(q.n_priv), 1};
@@ -562,52 +600,65 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest*
                                    static_cast<uint64_t>(a.Hkv) * a.D * 2,
                                    static_cast<uint64_t>(q.n_priv) * a.Hkv * a.D * 2};
       const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(kBN), 1u};
-      if (!encode_tmap_4d(&prm.tm_k[2], q.k_priv, dims, strides, box)) return cudaErrorInvalidValue;
-      if (!encode_tmap_4d(&prm.tm_v[2], q.v_priv, dims, strides, box)) return cudaErrorInvalidValue;
+      if (!encode_tmap_4d(&sp.tm_kp, q.k_priv, dims, strides, box)) return cudaErrorInvalidValue;
+      if (!encode_tmap_4d(&sp.tm_vp, q.v_priv, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    prm.k_tiles[0] = static_cast<const uint8_t*>(a.pin_k_tiles);
-    prm.v_tiles[0] = static_cast<const uint8_t*>(a.pin_v_tiles);
-    prm.k_tiles[1] = static_cast<const uint8_t*>(a.win_k_tiles);
-    prm.v_tiles[1] = static_cast<const uint8_t*>(a.win_v_tiles);
-    prm.head_stride[0] = a.pin_head_stride;
-    prm.head_stride[1] = a.win_head_stride;
-    prm.out = static_cast<__nv_bfloat16*>(q.out);
-    prm.part_o = a.part_o;
-    prm.part_ml = a.part_ml;
-    prm.st = a.st;
-    prm.err = a.err;
-    prm.layer = a.layer;
-    prm.P = a.P;
-    prm.F = a.F;
-    prm.n_priv = q.n_priv;
-    prm.Hq = a.Hq;
-    prm.G = G;
-    prm.rows = q.n_tok * G;
-    const int m_tiles = (prm.rows + kBM - 1) / kBM;
-    prm.rows_pad = m_tiles * kBM;
-    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
-    // Split the key sequence: about kTilesPerSplit 64-key tiles per CTA (the
-    // per-CTA set-up, Q load and partial write amortise over them), at most
-    // one wave of CTAs.
-    const int t_max = (a.P + kBN - 1) / kBN + (a.N * a.F + kBN - 1) / kBN + (q.n_priv + kBN - 1) / kBN;
-    const int wave = a.num_sms / (m_tiles * a.Hkv);
-    int splits = a.forced_splits > 0 ? a.forced_splits : (t_max + kTilesPerSplit - 1) / kTilesPerSplit;
-    if (a.forced_splits <= 0 && splits > wave) splits = wave;
-    splits = splits < 1 ? 1 : splits;
-    splits = splits > t_max ? t_max : splits;
-    splits = splits > a.max_splits ? a.max_splits : splits;
-    prm.n_splits = splits;
-    if (used_splits) *used_splits = splits;
-    cudaError_t e;
-    switch (a.D) {
-      case 64: e = launch_one<64>(prm, m_tiles, a.Hkv, s); break;
-      case 128: e = launch_one<128>(prm, m_tiles, a.Hkv, s); break;
-      case 256: e = launch_one<256>(prm, m_tiles, a.Hkv, s); break;
-      default: return cudaErrorInvalidValue;
-    }
-    if (e != cudaSuccess) return e;
+    sp.out = static_cast<__nv_bfloat16*>(q.out);
+    sp.tail_len = q.tail_len;
+    sp.n_priv = q.n_priv;
+    sp.rows = q.tokens * G;
+    sp.m_tiles = (sp.rows + kBM - 1) / kBM;
+    sp.row_base = m_total * kBM;
+    sp.tok_per_stream = q.tok_per_stream > 0 ? q.tok_per_stream : 1;
+    sp.tail_cap = q.tail_cap;
+    m_total += sp.m_tiles;
+    const int t = t_shared + (q.n_priv + kBN - 1) / kBN;
+    t_max = t > t_max ? t : t_max;
   }
-  return cudaSuccess;
+  if (nseg == 1) prm.seg[1].row_base = m_total * kBM;   // no second segment
+  if (!a.pin_k_tiles) {
+    prm.tm_k[0] = *a.tm_pin_k;
+    prm.tm_v[0] = *a.tm_pin_v;
+  }
+  if (!a.win_k_tiles) {
+    prm.tm_k[1] = *a.tm_slide_k;
+    prm.tm_v[1] = *a.tm_slide_v;
+  }
+  prm.k_tiles[0] = static_cast<const uint8_t*>(a.pin_k_tiles);
+  prm.v_tiles[0] = static_cast<const uint8_t*>(a.pin_v_tiles);
+  prm.k_tiles[1] = static_cast<const uint8_t*>(a.win_k_tiles);
+  prm.v_tiles[1] = static_cast<const uint8_t*>(a.win_v_tiles);
+  prm.head_stride[0] = a.pin_head_stride;
+  prm.head_stride[1] = a.win_head_stride;
+  prm.part_o = a.part_o;
+  prm.part_ml = a.part_ml;
+  prm.st = a.st;
+  prm.err = a.err;
+  prm.layer = a.layer;
+  prm.P = a.P;
+  prm.F = a.F;
+  prm.Hq = a.Hq;
+  prm.G = G;
+  prm.rows_pad = m_total * kBM;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
+  // Split the key sequence: about kTilesPerSplit 64-key tiles per CTA (the
+  // per-CTA set-up, Q load and partial write amortise over them), at most one
+  // wave of CTAs.
+  const int wave = a.num_sms / (m_total * a.Hkv);
+  int splits = a.forced_splits > 0 ? a.forced_splits : (t_max + kTilesPerSplit - 1) / kTilesPerSplit;
+  if (a.forced_splits <= 0 && splits > wave) splits = wave;
+  splits = splits < 1 ? 1 : splits;
+  splits = splits > t_max ? t_max : splits;
+  splits = splits > a.max_splits ? a.max_splits : splits;
+  splits = splits < 1 ? 1 : splits;
+  prm.n_splits = splits;
+  if (used_splits) *used_splits = splits;
+  switch (a.D) {
+    case 64: return launch_one<64>(prm, m_total, a.Hkv, s);
+    case 128: return launch_one<128>(prm, m_total, a.Hkv, s);
+    case 256: return launch_one<256>(prm, m_total, a.Hkv, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace rx

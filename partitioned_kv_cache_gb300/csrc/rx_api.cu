@@ -193,8 +193,9 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   const size_t tile = static_cast<size_t>(rx::tile_bytes(c.D));
   const size_t pin_b = round_up(static_cast<size_t>(c.L) * c.Hkv * h->T_pin * tile, 256);
   const size_t win_b = round_up(static_cast<size_t>(c.L) * c.Hkv * h->T_win * tile, 256);
-  const int max_tok = c.S_cap > c.tail_cap ? c.S_cap : c.tail_cap;
-  const size_t rows_pad = round_up(static_cast<size_t>(max_tok) * G, rx::kBM);
+  // Workspace rows: the action suffix plus a language batch (rx_attend_batch).
+  const size_t rows_pad = round_up(static_cast<size_t>(c.S_cap) * G, rx::kBM) +
+                          round_up(static_cast<size_t>(c.max_req) * G, rx::kBM);
   const size_t part_rows = static_cast<size_t>(c.Hkv) * h->max_splits * rows_pad;
   const size_t po_b = round_up(part_rows * c.D * sizeof(float), 256);
   const size_t pml_b = round_up(part_rows * sizeof(float2), 256);
@@ -339,41 +340,48 @@ rx_status rx_attend_suffix(rx_cache_t h, int layer, const void* q, const void* k
   if (!aligned16(q) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out))
     return fail(RX_ERR_ARG, "rx_attend_suffix: pointers must be 16-byte aligned");
   const rx::AttnLaunch a = make_launch(h, layer);
-  rx::AttnRequest r{q, k_dyn, v_dyn, out, S, S};
-  cudaError_t e = rx::launch_partitioned_attention(a, &r, 1, static_cast<cudaStream_t>(stream), nullptr);
+  rx::AttnSegment seg{q, k_dyn, v_dyn, out, S, S, nullptr, 1, 0};
+  cudaError_t e = rx::launch_partitioned_attention(a, &seg, 1, static_cast<cudaStream_t>(stream), nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "rx_attend_suffix: launch");
   return RX_OK;
   RX_GUARD_END
 }
 
-rx_status rx_attend_batch(rx_cache_t h, int layer, const rx_request* reqs, int nreq, void* stream) {
+rx_status rx_attend_batch(rx_cache_t h, int layer, const void* q_act, const void* k_dyn,
+                          const void* v_dyn, int S, void* out_act, const rx_stream_batch* lang,
+                          void* stream) {
   RX_GUARD_BEGIN
   if (!h) return fail(RX_ERR_ARG, "rx_attend_batch: null cache");
   const rx_config& c = h->cfg;
   if (layer < 0 || layer >= c.L) return fail(RX_ERR_LAYER, "rx_attend_batch: layer %d not in [0, %d)", layer, c.L);
-  if (nreq < 0 || (nreq > 0 && !reqs)) return fail(RX_ERR_ARG, "rx_attend_batch: bad request array");
-  if (nreq > c.max_req + 1 || nreq > rx::kMaxReq)
-    return fail(RX_ERR_CAPACITY, "rx_attend_batch: %d requests > max_req + 1 = %d", nreq, c.max_req + 1);
-  const int priv_cap = c.S_cap > c.tail_cap ? c.S_cap : c.tail_cap;
-  long long tot = 0;
-  rx::AttnRequest rr[rx::kMaxReq];
-  for (int i = 0; i < nreq; ++i) {
-    const rx_request& r = reqs[i];
-    if (r.n_tok < 1 || r.n_priv < 0) return fail(RX_ERR_ARG, "rx_attend_batch: request %d sizes", i);
-    if (r.n_tok > priv_cap) return fail(RX_ERR_CAPACITY, "rx_attend_batch: request %d n_tok = %d too large", i, r.n_tok);
-    if (r.n_priv > priv_cap) return fail(RX_ERR_CAPACITY, "rx_attend_batch: request %d n_priv = %d > %d", i, r.n_priv, priv_cap);
-    if (!r.q || !r.out || (r.n_priv > 0 && (!r.k_priv || !r.v_priv)))
-      return fail(RX_ERR_ARG, "rx_attend_batch: request %d null pointer", i);
-    if (!aligned16(r.q) || !aligned16(r.out) || (r.n_priv > 0 && (!aligned16(r.k_priv) || !aligned16(r.v_priv))))
-      return fail(RX_ERR_ARG, "rx_attend_batch: request %d pointers must be 16-byte aligned", i);
-    tot += r.n_tok;
-    rr[i] = rx::AttnRequest{r.q, r.k_priv, r.v_priv, r.out, r.n_tok, r.n_priv};
+  if (S < 0) return fail(RX_ERR_ARG, "rx_attend_batch: S < 0");
+  if (S > c.S_cap) return fail(RX_ERR_CAPACITY, "rx_attend_batch: S = %d > S_cap = %d", S, c.S_cap);
+  rx::AttnSegment segs[2];
+  int nseg = 0;
+  if (S > 0) {
+    if (!q_act || !k_dyn || !v_dyn || !out_act) return fail(RX_ERR_ARG, "rx_attend_batch: null action pointer");
+    if (!aligned16(q_act) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out_act))
+      return fail(RX_ERR_ARG, "rx_attend_batch: action pointers must be 16-byte aligned");
+    segs[nseg++] = rx::AttnSegment{q_act, k_dyn, v_dyn, out_act, S, S, nullptr, 1, 0};
   }
-  if (tot > static_cast<long long>(c.S_cap) + c.max_req)
-    return fail(RX_ERR_CAPACITY, "rx_attend_batch: %lld query tokens > S_cap + max_req", tot);
-  if (nreq == 0) return RX_OK;
+  if (lang && lang->B > 0) {
+    const rx_stream_batch& b = *lang;
+    if (b.T < 1) return fail(RX_ERR_ARG, "rx_attend_batch: T < 1");
+    if (static_cast<long long>(b.B) * b.T > c.max_req)
+      return fail(RX_ERR_CAPACITY, "rx_attend_batch: B*T = %lld > max_req = %d",
+                  static_cast<long long>(b.B) * b.T, c.max_req);
+    if (c.tail_cap < 1) return fail(RX_ERR_CAPACITY, "rx_attend_batch: the cache has tail_cap = 0");
+    if (!b.q || !b.k_tail || !b.v_tail || !b.tail_len || !b.out)
+      return fail(RX_ERR_ARG, "rx_attend_batch: null language pointer");
+    if (!aligned16(b.q) || !aligned16(b.k_tail) || !aligned16(b.v_tail) || !aligned16(b.out) ||
+        (reinterpret_cast<uintptr_t>(b.tail_len) & 3))
+      return fail(RX_ERR_ARG, "rx_attend_batch: language pointers misaligned");
+    segs[nseg++] = rx::AttnSegment{b.q, b.k_tail, b.v_tail, b.out, b.B * b.T, b.B * c.tail_cap,
+                                   b.tail_len, b.T, c.tail_cap};
+  }
+  if (nseg == 0) return RX_OK;
   const rx::AttnLaunch a = make_launch(h, layer);
-  cudaError_t e = rx::launch_partitioned_attention(a, rr, nreq, static_cast<cudaStream_t>(stream), nullptr);
+  cudaError_t e = rx::launch_partitioned_attention(a, segs, nseg, static_cast<cudaStream_t>(stream), nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "rx_attend_batch: launch");
   return RX_OK;
   RX_GUARD_END

@@ -94,15 +94,6 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
 constexpr int kBM = 128;   // query rows per CTA (one tcgen05 M=128 tile)
 constexpr int kBN = 64;    // keys per KV tile
 
-// One M-tile of queries: `rows` rows starting at row `row0` of a request.
-// Row r of a request is (token r / G, head g*G + r % G).
-struct TileDesc {
-  int req;        // request index (selects q / private-key maps and out)
-  int row0;       // first row of the tile within the request
-};
-
-constexpr int kMaxReq = 40;   // requests per batched launch (tensor maps in params)
-
 struct AttnLaunch {
   // Shared regions (pinned, window) of one layer.  Each is either pre-tiled
   // (pointers below non-null: bulk copies) or read through its tensor map.
@@ -126,19 +117,27 @@ struct AttnLaunch {
   int num_sms;
 };
 
-struct AttnRequest {
-  const void* q;      // bf16 [n_tok][Hq][D]
-  const void* k_priv; // bf16 [n_priv][Hkv][D] (may be null if n_priv == 0)
+// One group of query rows attending over [pinned; window; private keys].
+// Rows are (token, head-in-group) pairs: row r = token r / G, head g*G + r % G.
+struct AttnSegment {
+  const void* q;          // bf16 [tokens][Hq][D]
+  const void* k_priv;     // bf16 [n_priv][Hkv][D] (may be null if n_priv == 0)
   const void* v_priv;
-  void* out;          // bf16 [n_tok][Hq][D]
-  int n_tok;
-  int n_priv;
+  void* out;              // bf16 [tokens][Hq][D]
+  int tokens;             // query tokens
+  int n_priv;             // private keys
+  // Stream mask (language batches): token t belongs to stream t / tok_per_stream
+  // and sees private key j only if j / tail_cap is its stream and
+  // j % tail_cap < tail_len[stream].  tail_cap = 0 disables the mask.
+  const int* tail_len;
+  int tok_per_stream;
+  int tail_cap;
 };
 
-// Encode the tensor maps of every request and launch the attention kernel
-// (plus the split merge when more than one split is used).
-cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnRequest* reqs,
-                                         int nreq, cudaStream_t s, int* used_splits);
+// Launch the attention kernel over one or two segments (plus the split merge
+// when more than one split is used).  Both segments read the same shared K/V.
+cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment* segs, int nseg,
+                                         cudaStream_t s, int* used_splits);
 
 // Tensor-map encoding through the driver entry point (no -lcuda link).
 bool encode_tmap_4d(CUtensorMap* tm, const void* base, const uint64_t dims[4],

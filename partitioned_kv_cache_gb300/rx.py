@@ -37,9 +37,10 @@ class RxConfig(ctypes.Structure):
                 ("L", "Hq", "Hkv", "D", "P_cap", "N", "F", "S_cap", "tail_cap", "max_req")]
 
 
-class RxRequest(ctypes.Structure):
-    _fields_ = [("q", ctypes.c_void_p), ("k_priv", ctypes.c_void_p), ("v_priv", ctypes.c_void_p),
-                ("out", ctypes.c_void_p), ("n_tok", ctypes.c_int), ("n_priv", ctypes.c_int)]
+class RxStreamBatch(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_tail", ctypes.c_void_p), ("v_tail", ctypes.c_void_p),
+                ("tail_len", ctypes.c_void_p), ("out", ctypes.c_void_p), ("B", ctypes.c_int),
+                ("T", ctypes.c_int)]
 
 
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -49,7 +50,7 @@ _sigs = {
     "rx_pin_prefix": (_i, [_vp, _vp, _vp, _i, _vp]),
     "rx_push_frame": (_i, [_vp, _vp, _vp, ctypes.POINTER(_i), _vp]),
     "rx_attend_suffix": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, _vp]),
-    "rx_attend_batch": (_i, [_vp, _i, ctypes.POINTER(RxRequest), _i, _vp]),
+    "rx_attend_batch": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, ctypes.POINTER(RxStreamBatch), _vp]),
     "rx_ada_gamma": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp]),
     "rx_adarmsnorm": (_i, [_vp, _vp, _i, _i, _f, _vp, _vp]),
     "rx_get_state": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i),
@@ -155,21 +156,34 @@ class Cache:
                                      _stream(stream)), "rx_attend_suffix")
         return out
 
-    def attend_batch(self, layer: int, requests: Sequence[Tuple], stream=None) -> List[torch.Tensor]:
-        """requests: (q [n][Hq][D], k_priv [t][Hkv][D] or None, v_priv, out or None)."""
-        arr = (RxRequest * max(1, len(requests)))()
-        outs = []
-        for i, r in enumerate(requests):
-            q, kp, vp = r[0], r[1], r[2]
-            out = r[3] if len(r) > 3 and r[3] is not None else torch.empty_like(q)
-            n_priv = 0 if kp is None else kp.shape[0]
-            arr[i] = RxRequest(_ptr(q, name="q"), _ptr(kp, name="k_priv") if n_priv else None,
-                               _ptr(vp, name="v_priv") if n_priv else None, _ptr(out, name="out"),
-                               q.shape[0], n_priv)
-            outs.append(out)
-        _check(_lib.rx_attend_batch(self._h, layer, arr, len(requests), _stream(stream)),
-               "rx_attend_batch")
-        return outs
+    def attend_batch(self, layer: int, action=None, lang=None, out_act: Optional[torch.Tensor] = None,
+                     out_lang: Optional[torch.Tensor] = None, stream=None):
+        """One launch for an action suffix and a batch of language streams.
+
+        action: (q [S][Hq][D], k_dyn [S][Hkv][D], v_dyn) or None.
+        lang: (q [B][T][Hq][D], k_tail [B][tail_cap][Hkv][D], v_tail,
+               tail_len int32 CUDA tensor [B]) or None.
+        Returns (out_act or None, out_lang or None).
+        """
+        S, qa, kd, vd = 0, None, None, None
+        if action is not None:
+            qa, kd, vd = action
+            S = qa.shape[0]
+            if out_act is None:
+                out_act = torch.empty_like(qa)
+        batch = None
+        if lang is not None:
+            ql, kt, vt, tl = lang
+            if out_lang is None:
+                out_lang = torch.empty_like(ql)
+            batch = RxStreamBatch(_ptr(ql, name="q_lang"), _ptr(kt, name="k_tail"),
+                                  _ptr(vt, name="v_tail"), _ptr(tl, torch.int32, "tail_len"),
+                                  _ptr(out_lang, name="out_lang"), ql.shape[0], ql.shape[1])
+        _check(_lib.rx_attend_batch(self._h, layer, _ptr(qa, name="q"), _ptr(kd, name="k_dyn"),
+                                    _ptr(vd, name="v_dyn"), S, _ptr(out_act, name="out_act"),
+                                    ctypes.byref(batch) if batch is not None else None,
+                                    _stream(stream)), "rx_attend_batch")
+        return (out_act if action is not None else None), (out_lang if lang is not None else None)
 
     def get_state(self, stream=None) -> Tuple[int, int, int]:
         h, v, p = _i(0), _i(0), ctypes.c_longlong(0)

@@ -88,5 +88,5 @@ def test_cache_calls_reject_null_handle(lib):
     assert L.rx_pin_prefix(None, None, None, 0, None) == -1
     assert L.rx_push_frame(None, None, None, None, None) == -1
     assert L.rx_attend_suffix(None, 0, None, None, None, 1, None, None) == -1
-    assert L.rx_attend_batch(None, 0, None, 0, None) == -1
+    assert L.rx_attend_batch(None, 0, None, None, None, 0, None, None, None) == -1
     assert L.rx_set_attn_splits(None, 0) == -1
