@@ -23,9 +23,14 @@
 //     online softmax in the exp2 domain; O is rescaled in TMEM only when the
 //     running maximum grows by more than 2^8 (otherwise the stale maximum is
 //     kept: exact after the final division by the row sum).
-//   * The key sequence is split across CTAs (gridDim.y).  Each split writes an
-//     fp32 partial (O, m, l); a merge kernel combines them with the global
-//     maximum.  With a single split the CTA writes the bf16 output directly.
+//   * The key sequence is split across CTAs (gridDim.y).  When the splits of an
+//     M-tile form one thread-block cluster (up to kMaxClusterSplits), each CTA
+//     parks its fp32 (O, m, l) in its own shared memory and the cluster
+//     combines them through distributed shared memory, every CTA finishing a
+//     disjoint set of 32-column chunks of the bf16 output: no partials leave
+//     the chip and no second kernel runs.  Beyond that size each split writes
+//     an fp32 partial to global memory and a merge kernel combines them.  With
+//     a single split the CTA writes the bf16 output directly.
 //
 // Warp roles (224 threads): warp 0 = copy producer, warp 1 = TMEM allocator and
 // Q K^T issuer, warp 6 = P V issuer, warps 2..5 = softmax and epilogue (TMEM
@@ -50,6 +55,7 @@ namespace {
 constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kTilesPerSplit = 8;            // target key tiles per split
+constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a cluster
 
 template <int D>
 struct Layout {
@@ -73,7 +79,7 @@ struct Layout {
 
 // Barrier indices: Q, ring full[NS], ring empty[NS], S full[2], P full[2],
 // PV done[2], drain.
-enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39 };
+enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39, B_RECV = 40 };
 
 // One group of query rows: the action suffix, or a dense batch of language
 // streams.  Its M-tiles occupy workspace rows [row_base, row_base + m_tiles*128).
@@ -107,6 +113,7 @@ struct AttnParams {
   int Hq, G;
   int rows_pad;          // workspace rows of all segments
   int n_splits;
+  int fused;             // 1: the splits of an M-tile form a cluster and merge on chip
   float scale_log2;      // log2(e) / sqrt(D)
 };
 
@@ -145,6 +152,49 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Park this thread's row of the split's normalised partial O / l (bf16) and
+// (m, l) in shared memory for the cluster merge.  Layout at `os`: [D/16
+// halves][8 column pairs][128 rows] of bf16x2, so a half is one contiguous
+// 4 KB block (one bulk copy) and a warp's 4-byte stores cover 128 contiguous
+// bytes; (m, l) follow at os + D*256.  With have_o == false the row is zeros
+// (an empty split, l = 0).  Warp-collective (TMEM loads).
+template <int D>
+__device__ __forceinline__ void park_partial(uint32_t os, uint32_t t_row, int row, float m, float l,
+                                             bool have_o) {
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    float o[32];
+    if (have_o) {
+      tmem_ld32(t_row + c, o);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0.f;
+    }
+#pragma unroll
+    for (int pr = 0; pr < 16; ++pr) {
+      const int col = c + 2 * pr;   // columns col, col+1
+      const uint32_t a = os + (col / 16) * 4096 + ((col % 16) / 2) * 512 + row * 4;
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(pack_bf16x2(o[2 * pr] * inv, o[2 * pr + 1] * inv))
+                   : "memory");
+    }
+  }
+  const uint32_t mla = os + D * 256 + row * 8;
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(mla), "f"(m), "f"(l) : "memory");
+  fence_proxy_async_smem();   // the halves leave through the copy engine (async proxy)
+}
+
+// Push `bytes` of this CTA's shared memory to shared memory of a cluster
+// peer (addresses from dsmem_map), completion counted on the peer's mbarrier.
+__device__ __forceinline__ void bulk_push(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                          uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
 
@@ -190,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(BAR(B_PV + i), 1);
     }
     mbar_init(BAR(B_DRAIN), 2);   // one commit from each MMA issuer
+    mbar_init(BAR(B_RECV), 1);    // cluster merge: partial halves pushed to this CTA
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -450,6 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                                  pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
           }
         }
+      } else if (p.fused) {
+        park_partial<D>(base + Lay::OFF_Q, tO + lane_off, row, m_used, l, true);
       } else {
         // Partial O is stored column-major per split ([D][rows_pad]): for each
         // column the 32 lanes of a warp write 32 consecutive rows (128 B).
@@ -465,9 +518,106 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         if (row_valid) p.part_ml[part_idx] = make_float2(m_used, l);
       }
+    } else if (p.fused) {
+      // empty (or abandoned) split: zeros with l = 0 contribute nothing
+      park_partial<D>(base + Lay::OFF_Q, tO + lane_off, row, -INFINITY, 0.f, false);
     } else if (n == 0 && row_valid && p.n_splits > 1) {
       p.part_ml[part_idx] = make_float2(-INFINITY, 0.f);   // empty split: merge skips it
     }
+  }
+
+  if (p.fused) {
+    // ---------------------------------------------------------- cluster merge
+    // Each CTA owns the 16-column halves rank, rank + C, ... of the output.
+    // After barrier 1 every CTA pushes each of its parked halves (4 KB) into
+    // the owner's receive slot [local half][source rank]; the owner combines
+    // them from its own shared memory.  All threads of all CTAs of the
+    // cluster pass both barriers, whatever path they took above.
+    const int C = p.n_splits;
+    const uint32_t rank = cluster_ctarank();
+    const int owned = (D / 16 - static_cast<int>(rank) + C - 1) / C;
+    const uint32_t os_local = base + Lay::OFF_Q;
+    const uint32_t recv_local = os_local + D * 256 + 1024;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(BAR(B_RECV), owned * C * 4096);
+    __syncwarp();
+    cluster_sync_all();
+    if (threadIdx.x == 0) {
+      for (int half = 0; half < D / 16; ++half) {
+        const uint32_t owner = static_cast<uint32_t>(half % C);
+        const uint32_t slot = static_cast<uint32_t>((half / C) * C) + rank;
+        bulk_push(dsmem_map(recv_local + slot * 4096, owner), os_local + half * 4096, 4096,
+                  dsmem_map(BAR(B_RECV), owner));
+      }
+    }
+    if (warp >= 2 && warp <= 5) {
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;
+      const int Rs = mt * kBM + row;
+      const uint32_t ml_local = os_local + D * 256 + row * 8;
+      float ms[kMaxClusterSplits], ws[kMaxClusterSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+        ws[s2] = 0.f;
+        ms[s2] = -INFINITY;
+        if (s2 < C) {
+          const float2 v = dsmem_ld_f32x2(dsmem_map(ml_local, s2));
+          if (v.y > 0.f) {
+            ms[s2] = v.x;
+            ws[s2] = v.y;
+            M = fmaxf(M, v.x);
+          }
+        }
+      }
+      // Weight of split s: 2^(m_s - M) l_s / L (the parked partials are O_s / l_s).
+      float L = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+        const float w = ws[s2] > 0.f ? exp2f(ms[s2] - M) * ws[s2] : 0.f;
+        L += w;
+        ws[s2] = w;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) ws[s2] *= inv;
+      const bool row_valid = Rs < sg.rows;
+      const int tok = Rs / p.G, h = g * p.G + Rs % p.G;
+      const bool got = warp_wait(BAR(B_RECV), 0, abort_flag);
+      for (int k = 0; got && k < owned; ++k) {
+        const int half = static_cast<int>(rank) + k * C;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+          if (s2 < C) {
+            const uint32_t src = recv_local + (k * C + s2) * 4096 + row * 4;
+#pragma unroll
+            for (int pr = 0; pr < 8; ++pr) {
+              uint32_t v;
+              asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src + pr * 512) : "memory");
+              acc[2 * pr] = fmaf(ws[s2], __uint_as_float(v << 16), acc[2 * pr]);
+              acc[2 * pr + 1] = fmaf(ws[s2], __uint_as_float(v & 0xFFFF0000u), acc[2 * pr + 1]);
+            }
+          }
+        }
+        if (row_valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D + half * 16);
+          d4[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+          d4[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                             pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+        }
+      }
+    }
+    // Every push into this CTA must land before it leaves barrier 2 (an
+    // abandoned wait above still drains here, bounded).
+    if (threadIdx.x == 0) {
+      volatile int no_abort = 0;
+      mbar_wait(BAR(B_RECV), 0, &no_abort);
+    }
+    __syncwarp();
+    cluster_sync_all();   // peers may still read this CTA's shared memory until here
   }
 
   tc_fence_before();
@@ -559,18 +709,73 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Lay::ALLOC);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(m_tiles, prm.n_splits, Hkv);
-  cudaError_t e = launch_k(attn_kernel<D>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
+  cudaError_t e;
+  if (prm.fused) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Lay::ALLOC;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = prm.n_splits;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, attn_kernel<D>, prm);
+    count_launch();
+  } else {
+    e = launch_k(attn_kernel<D>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess || prm.n_splits == 1) return e;
+  if (e != cudaSuccess || prm.n_splits == 1 || prm.fused) return e;
   dim3 mgrid(prm.rows_pad / 32, D / 32, Hkv);
   e = launch_k(attn_merge_kernel<D>, mgrid, dim3(128), 0, s, static_cast<const float*>(prm.part_o),
                static_cast<const float2*>(prm.part_ml), prm.seg[0].out, prm.seg[0].rows,
                prm.seg[1].out, prm.seg[1].rows, prm.seg[1].row_base, prm.rows_pad, prm.n_splits,
                prm.Hq, prm.G);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Largest cluster of attention CTAs (one per SM) the device can co-schedule,
+// capped at kMaxClusterSplits; 1 if clusters are unavailable.
+template <int D>
+int max_cluster_splits() {
+  static int cached = -1;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached >= 0) return cached;
+  cached = 1;
+  cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::ALLOC);
+  cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  for (int c = kMaxClusterSplits; c >= 2; c /= 2) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, c, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Layout<D>::ALLOC;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = c;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<D>, &cfg) == cudaSuccess && n >= 1) {
+      cached = c;
+      break;
+    }
+  }
+  cudaGetLastError();
+  return cached;
 }
 
 }  // namespace
@@ -649,9 +854,20 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   if (a.forced_splits <= 0 && splits > wave) splits = wave;
   splits = splits < 1 ? 1 : splits;
   splits = splits > t_max ? t_max : splits;
-  splits = splits > a.max_splits ? a.max_splits : splits;
+  int cmax = 1;
+  switch (a.D) {
+    case 64: cmax = max_cluster_splits<64>(); break;
+    case 128: cmax = max_cluster_splits<128>(); break;
+    case 256: cmax = max_cluster_splits<256>(); break;
+    default: return cudaErrorInvalidValue;
+  }
+  // Prefer an on-chip (cluster) merge: cap the automatic split count there.
+  if (a.forced_splits <= 0 && splits > cmax && cmax >= 2) splits = cmax;
+  const bool fused = splits >= 2 && splits <= cmax;
+  if (!fused) splits = splits > a.max_splits ? a.max_splits : splits;
   splits = splits < 1 ? 1 : splits;
   prm.n_splits = splits;
+  prm.fused = fused ? 1 : 0;
   if (used_splits) *used_splits = splits;
   switch (a.D) {
     case 64: return launch_one<64>(prm, m_total, a.Hkv, s);

@@ -77,7 +77,7 @@ def test_before_any_push_attends_pinned_and_dynamic_only(rx):
     cache.close()
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 0])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 16, 18, 0])
 def test_split_count_does_not_change_the_result(rx, splits):
     wl = W.WORKLOADS["c2"]
     seed = 3
