@@ -50,14 +50,22 @@ def load_peaks():
 
 
 def attn_flops(wl: W.Workload) -> float:
-    """Algorithmic FLOPs of one attention call (full window): 4*Hq*S*Lk*D."""
-    return 4.0 * wl.Hq * wl.S * wl.keys_full * wl.D
+    """Algorithmic FLOPs of one attention call (full window): 4*Hq*S*Lk*D for
+    the suffix, plus 4*Hq*(cached + mean tail)*D per language stream."""
+    f = 4.0 * wl.Hq * wl.S * wl.keys_full * wl.D
+    if wl.n_lang:
+        f += wl.n_lang * 4.0 * wl.Hq * (wl.cached + wl.tail_max / 2.0) * wl.D
+    return f
 
 
 def describe(wl: W.Workload) -> str:
-    return ("%s: %d layers, %d q / %d kv heads, head_dim %d, pinned %d, window %d x %d, "
-            "suffix %d, %d denoising steps per tick, AdaRMSNorm d=%d" %
-            (wl.name, wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S, wl.steps, wl.d_model))
+    d = ("%s: %d layers, %d q / %d kv heads, head_dim %d, pinned %d, window %d x %d, "
+         "suffix %d, %d denoising steps per tick, AdaRMSNorm d=%d" %
+         (wl.name, wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S, wl.steps, wl.d_model))
+    if wl.n_lang:
+        d += ("; plus %d one-token language streams with private tails U{0..%d} in the same "
+              "attention launch" % (wl.n_lang, wl.tail_max))
+    return d
 
 
 # ---------------------------------------------------------------------------
@@ -121,6 +129,7 @@ def oracle_sample(wl: W.Workload, seed: int, denoise_steps: int):
     """Time the oracle over one frame push + `denoise_steps` denoising steps of
     all layers (gamma, AdaRMSNorm, attention, AdaRMSNorm).  Returns
     (denoise-steps/s, seconds, description)."""
+    from oracle.attention import shared_cache_attention
     from oracle.pipeline import OracleStream
     st = OracleStream(wl, seed)
     for t in range(wl.N):
@@ -128,10 +137,16 @@ def oracle_sample(wl: W.Workload, seed: int, denoise_steps: int):
     tick = wl.N
     t0 = time.perf_counter()
     st.push(tick)
+    f = W.bf16_bits_to_f64
     for k in range(denoise_steps):
         for l in range(wl.L):
             st.norm(tick, k % wl.steps, l, 0)
             st.attend(tick, k % wl.steps, l)
+            if wl.n_lang:   # the language streams of the shared-cache workload
+                q, tk, tv, ln = W.lang_requests(wl, seed, tick, k % wl.steps, l)
+                ks, vs = st.regions(l, f(tk[0, :0]), f(tv[0, :0]))
+                shared_cache_attention(ks[:-1], vs[:-1], [(f(q[b]), f(tk[b, :ln[b]]), f(tv[b, :ln[b]]))
+                                                          for b in range(wl.n_lang)])
             st.norm(tick, k % wl.steps, l, 1)
     dt = time.perf_counter() - t0
     return denoise_steps / dt, dt, ("1 frame push + %d denoising steps x %d layers of %s"
@@ -187,7 +202,8 @@ def run_ours(args, wl):
         return (torch.randn(*shape, generator=g, device=dev) * scale).to(torch.bfloat16)
 
     L, S, Hq, Hkv, D, K = wl.L, wl.S, wl.Hq, wl.Hkv, wl.D, wl.steps
-    cache = rx.Cache(L, Hq, Hkv, D, wl.P, wl.N, wl.F, S)
+    B = wl.n_lang
+    cache = rx.Cache(L, Hq, Hkv, D, wl.P, wl.N, wl.F, S, wl.tail_cap, B)
     if args.splits:
         cache.set_attn_splits(args.splits)
     cache.pin_prefix(randn_bf16(L, wl.P, Hkv, D), randn_bf16(L, wl.P, Hkv, D))
@@ -205,11 +221,25 @@ def run_ours(args, wl):
     b1 = randn_bf16(n_sets, wl.hidden, scale=0.02)
     W2 = randn_bf16(n_sets, wl.d_model, wl.hidden, scale=0.02)
     b2 = randn_bf16(n_sets, wl.d_model, scale=0.02)
+    if B:   # language streams sharing the cache: 1 query token each, private tails
+        ql = randn_bf16(NSLOT, K, L, B, 1, Hq, D)
+        ol = torch.empty_like(ql)
+        tails_k = randn_bf16(L, B, wl.tail_cap, Hkv, D)
+        tails_v = randn_bf16(L, B, wl.tail_cap, Hkv, D)
+        tail_len = torch.randint(0, wl.tail_max + 1, (L, B), generator=g, device=dev, dtype=torch.int32)
     tk = torch.tensor(W.timesteps(wl), device=dev)
     state = (torch.rand(NSLOT, K, wl.state_dim, generator=g, device=dev) * 2 - 1).contiguous()
     gamma = torch.empty((n_sets, K, wl.d_model), dtype=torch.float32, device=dev)
     for t in range(wl.N):   # fill the window before timing (steady state)
         cache.push_frame(*frames[t % NSLOT])
+
+    def attend(slot, k, l):
+        if B:
+            cache.attend_batch(l, (q[slot, k, l], kd[slot, k, l], vd[slot, k, l]),
+                               (ql[slot, k, l], tails_k[l], tails_v[l], tail_len[l]),
+                               out_act=o[slot, k, l], out_lang=ol[slot, k, l])
+        else:
+            cache.attend_suffix(l, q[slot, k, l], kd[slot, k, l], vd[slot, k, l], out=o[slot, k, l])
 
     def tick(slot):
         rx.ada_gamma(tk, state[slot], W1, b1, W2, b2, wl.emb_dim, out=gamma)
@@ -217,13 +247,13 @@ def run_ours(args, wl):
         for k in range(K):
             for l in range(L):
                 rx.adarmsnorm(x[slot, k, l, 0], gamma[2 * l, k], wl.eps, out=y[slot, k, l, 0])
-                cache.attend_suffix(l, q[slot, k, l], kd[slot, k, l], vd[slot, k, l], out=o[slot, k, l])
+                attend(slot, k, l)
                 rx.adarmsnorm(x[slot, k, l, 1], gamma[2 * l + 1, k], wl.eps, out=y[slot, k, l, 1])
 
     def attn_only(slot):
         for k in range(K):
             for l in range(L):
-                cache.attend_suffix(l, q[slot, k, l], kd[slot, k, l], vd[slot, k, l], out=o[slot, k, l])
+                attend(slot, k, l)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -296,35 +326,49 @@ def run_ours(args, wl):
     achieved = fl / (attn_us * 1e-6) / 1e12
     peak_tf = float(peaks["bf16_tflops"])
 
-    # ---------------- append and AdaRMSNorm bandwidth ----------------
+    # ---------------- append and AdaRMSNorm bandwidth (graph replays) ----------------
     kern = {}
     nfr = max(2, int(np.ceil(2 * 129e6 / (2 * L * wl.F * Hkv * D * 2))))
     pool = [(randn_bf16(L, wl.F, Hkv, D), randn_bf16(L, wl.F, Hkv, D)) for _ in range(nfr)]
     with torch.cuda.stream(stream):
         for fr in pool:
             cache.push_frame(*fr)
+    torch.cuda.synchronize()
+    p_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(p_graph, stream=stream):
+        for fr in pool:
+            cache.push_frame(*fr)
+    with torch.cuda.stream(stream):
+        p_graph.replay()
         b0 = torch.cuda.Event(enable_timing=True)
         b1 = torch.cuda.Event(enable_timing=True)
         b0.record(stream)
-        for fr in pool:
-            cache.push_frame(*fr)
+        for _ in range(3):
+            p_graph.replay()
         b1.record(stream)
     b1.synchronize()
-    app_us = b0.elapsed_time(b1) * 1e3 / nfr
+    app_us = b0.elapsed_time(b1) * 1e3 / (3 * nfr)
     app_bytes = 2.0 * 2 * L * wl.F * Hkv * D * 2
     kern["ring_append"] = {"us": app_us, "bytes": app_bytes, "GB/s": app_bytes / app_us / 1e3,
                            "frac_hbm": app_bytes / app_us / 1e3 / float(peaks["hbm_gbs"]),
-                           "note": "one push of all %d layers, frames rotate over %d buffers" % (L, nfr)}
+                           "note": "one push of all %d layers (read + write of K and V), graph of %d "
+                                   "pushes over distinct frames (> 2x L2)" % (L, nfr)}
     rows_bw = S * L * 2 * 64
     xs = [randn_bf16(rows_bw, wl.d_model) for _ in range(2)]
     ys = torch.empty_like(xs[0])
     with torch.cuda.stream(stream):
         rx.adarmsnorm(xs[0], gamma[0, 0], wl.eps, out=ys)
+    torch.cuda.synchronize()
+    n_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(n_graph, stream=stream):
+        for i in range(10):
+            rx.adarmsnorm(xs[i % 2], gamma[0, 0], wl.eps, out=ys)
+    with torch.cuda.stream(stream):
+        n_graph.replay()
         c0 = torch.cuda.Event(enable_timing=True)
         c1 = torch.cuda.Event(enable_timing=True)
         c0.record(stream)
-        for i in range(10):
-            rx.adarmsnorm(xs[i % 2], gamma[0, 0], wl.eps, out=ys)
+        n_graph.replay()
         c1.record(stream)
     c1.synchronize()
     nrm_us = c0.elapsed_time(c1) * 1e3 / 10
@@ -407,7 +451,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="c3", choices=["c2", "c3", "c4"])
+    ap.add_argument("--workload", default="c3", choices=["c2", "c3", "c4", "c5"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--splits", type=int, default=0, help="split-KV partitions (0 = automatic)")

@@ -54,7 +54,7 @@ namespace {
 
 constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kTilesPerSplit = 8;            // target key tiles per split
+constexpr int kTilesPerSplit = 3;            // target key tiles per split (on-chip merge)
 constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a cluster
 
 template <int D>
