@@ -39,6 +39,23 @@ METRIC = "partitioned-attn denoise-steps/s; TFLOP/s & HBM GB/s as % of GB300 pea
 UNIT = "denoise-steps/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
+# launch from the ncu capture summarised in profiles/attn_kernel_c3.md.  It is
+# reported only while the kernel source still matches the one captured.
+ATTN_TRAFFIC = {"sha256_16": "d50524a975b94d6b", "workload": "c3", "bytes": 2.503e6}
+
+
+def attn_traffic(wl_key: str):
+    import hashlib
+    src = os.path.join(ROOT, "partitioned_kv_cache_gb300", "csrc", "partitioned_attn.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if sha == ATTN_TRAFFIC["sha256_16"] and wl_key == ATTN_TRAFFIC["workload"]:
+        return ATTN_TRAFFIC["bytes"]
+    return None
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -430,7 +447,7 @@ def run_ours(args, wl):
                             wl.cached * Hkv * D * 4 / 1e6, K),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": None,
+                     "frac": achieved / peak_tf, "traffic": attn_traffic(args.workload),
                      "kernel": "partitioned attention (split-KV kernel + merge), %.2f us per call, "
                                "%.3g algorithmic FLOP per call (4*Hq*S*Lk*D)" % (attn_us, fl),
                      "peak_kind": "%s bf16 dense burst" % peak_kind},
