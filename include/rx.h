@@ -124,6 +124,16 @@ rx_status rx_attend_suffix(rx_cache_t cache, int layer, const void* q,
                            const void* k_dyn, const void* v_dyn, int S,
                            void* out, void* stream);
 
+/* Block-causal variant of rx_attend_suffix (the other plain reading of the
+ * attention-mask figure of "Reflex ...", §III "System architecture"): the
+ * first n_state suffix tokens (the state block) attend over the cached
+ * regions and only the state block's own dynamic keys, k_dyn[0, n_state);
+ * the remaining (action) tokens attend over every key.  n_state = 0 is
+ * rx_attend_suffix.  0 <= n_state <= S.  Errors as rx_attend_suffix. */
+rx_status rx_attend_suffix_block_causal(rx_cache_t cache, int layer, const void* q,
+                                        const void* k_dyn, const void* v_dyn, int S,
+                                        int n_state, void* out, void* stream);
+
 /* A dense batch of language streams sharing the cache: B streams of T query
  * tokens each, every stream with its own appended keys (its private tail). */
 typedef struct rx_stream_batch {
@@ -156,6 +166,38 @@ rx_status rx_attend_batch(rx_cache_t cache, int layer, const void* q_act,
                           const void* k_dyn, const void* v_dyn, int S,
                           void* out_act, const rx_stream_batch* lang,
                           void* stream);
+
+/* Append one token to each active language stream's private tail (cross-frame
+ * continuous batching, "OxyGen ...", §"Core method": a stream's KV cache grows
+ * by one entry per decoded token and the stream resumes across frames).
+ * For every b < B with active[b] != 0 (or every b when active is NULL):
+ *   if tail_len[b] < tail_cap: k_tail[b][tail_len[b]] = k_new[b],
+ *                              v_tail[b][tail_len[b]] = v_new[b], tail_len[b] += 1
+ *   else: the token is dropped and bit 0 of *overflow is set (a full stream
+ *         must be retired; a host scheduler resets tail_len[b] = 0 to reuse it).
+ * k_tail, v_tail: bf16 [B][tail_cap][Hkv][D]; k_new, v_new: bf16 [B][Hkv][D];
+ * tail_len: DEVICE int32 [B] (read and advanced on the device, so a captured
+ * graph keeps appending); active: DEVICE int32 [B] or NULL; overflow: DEVICE
+ * int32 or NULL.  Hkv*D % 8 == 0.  Errors: RX_ERR_ARG, RX_ERR_CUDA. */
+rx_status rx_tail_append(void* k_tail, void* v_tail, int* tail_len, const void* k_new,
+                         const void* v_new, const int* active, int B, int tail_cap,
+                         int Hkv, int D, int* overflow, void* stream);
+
+/* Ring-state snapshot / restore (execution-state capsules as in the FlashRT
+ * summary page: snapshot and restore of the named static buffers).  A
+ * snapshot holds the pinned prefix, the window, the device-side ring state
+ * and the host-side counters; restoring it and then pushing the same frames
+ * reproduces every later output bit for bit.
+ * rx_snapshot_bytes: size of a snapshot of this cache.
+ * rx_snapshot: dst is caller-owned DEVICE memory of that size; the copy is
+ *   enqueued on `stream` after the work already there.
+ * rx_restore: src must hold a snapshot of a cache with the same rx_config;
+ *   synchronises `stream` to validate it, then enqueues the copies.
+ * Errors: RX_ERR_ARG (null, or a snapshot of another configuration),
+ * RX_ERR_CUDA. */
+rx_status rx_snapshot_bytes(rx_cache_t cache, long long* bytes);
+rx_status rx_snapshot(rx_cache_t cache, void* dst, void* stream);
+rx_status rx_restore(rx_cache_t cache, const void* src, void* stream);
 
 /* Gamma of AdaRMSNorm ("Reflex ...", §III Eq. 2 and "Model components"):
  * for every weight set i and conditioning vector k

@@ -84,6 +84,27 @@ def partitioned_attention(q, k_regions: Sequence, v_regions: Sequence) -> np.nda
     return full_attention(q, K, V)
 
 
+def block_causal_attention(q, k_regions: Sequence, v_regions: Sequence, n_state: int) -> np.ndarray:
+    """Eq. (1) with a block-causal suffix (the other plain reading of the
+    attention-mask figure of "Reflex: ...", §III "System architecture"): the
+    last region is the dynamic suffix; its first ``n_state`` tokens (the state
+    block) see the cached regions and only the state block's own keys, while
+    the remaining (action) tokens see every key.  n_state = 0 is Eq. (1).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    S = q.shape[0]
+    ks = [np.asarray(k, dtype=np.float64) for k in k_regions]
+    vs = [np.asarray(v, dtype=np.float64) for v in v_regions]
+    n_state = max(0, min(int(n_state), S))
+    out = np.empty(q.shape, dtype=np.float64)
+    if n_state:
+        out[:n_state] = partitioned_attention(q[:n_state], ks[:-1] + [ks[-1][:n_state]],
+                                              vs[:-1] + [vs[-1][:n_state]])
+    if n_state < S:
+        out[n_state:] = partitioned_attention(q[n_state:], ks, vs)
+    return out
+
+
 def region_split_attention(q, k_regions: Sequence, v_regions: Sequence) -> np.ndarray:
     """Proposition A.1, evaluated region by region.
 

@@ -95,6 +95,7 @@ struct SegParams {
   int m_tiles;
   int tok_per_stream;    // stream mask: query tokens per stream
   int tail_cap;          // stream mask: private keys per stream; 0 = no mask
+  int state_tokens;      // block-causal: tokens below see private keys [0, state_tokens) only
 };
 
 struct AttnParams {
@@ -394,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const bool row_valid = Rs < sg.rows;
     const int R = sg.row_base + Rs;                    // row within the workspace
     const size_t part_idx = (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad + R;
-    // Stream mask: this row's stream sees private keys [lo, hi) only.
+    // Private-key window of this row: its stream's tail (stream mask) or the
+    // state block's own keys (block-causal suffix); [0, n_priv) otherwise.
     int lo = 0, hi = sg.n_priv;
     if (sg.tail_cap > 0) {
       lo = hi = 0;
@@ -404,6 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         hi = lo + min(max(sg.tail_len[b], 0), sg.tail_cap);
       }
     }
+    if (sg.state_tokens > 0 && Rs / p.G < sg.state_tokens) hi = min(hi, sg.state_tokens);
+    const bool priv_masked = sg.tail_cap > 0 || sg.state_tokens > 0;
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = n > 0;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       tmem_ld32(tS + st * kBN + lane_off, s);
       tmem_ld32(tS + st * kBN + 32 + lane_off, s + 32);
       const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv);
-      if (ti.region == 2 && sg.tail_cap > 0) {   // private keys of other streams are not keys
+      if (ti.region == 2 && priv_masked) {   // private keys outside this row's window
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
           const int key = ti.key0 + c;
@@ -816,6 +820,7 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
     sp.row_base = m_total * kBM;
     sp.tok_per_stream = q.tok_per_stream > 0 ? q.tok_per_stream : 1;
     sp.tail_cap = q.tail_cap;
+    sp.state_tokens = q.state_tokens;
     m_total += sp.m_tiles;
     const int t = t_shared + (q.n_priv + kBN - 1) / kBN;
     t_max = t > t_max ? t : t_max;

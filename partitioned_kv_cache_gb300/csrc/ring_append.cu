@@ -95,6 +95,29 @@ __global__ void __launch_bounds__(kThreads) pack_tiles_kernel(
   }
 }
 
+// One CTA per stream: append k_new[b] / v_new[b] at position tail_len[b].
+__global__ void __launch_bounds__(64) tail_append_kernel(
+    uint4* __restrict__ k_tail, uint4* __restrict__ v_tail, int* __restrict__ tail_len,
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, const int* __restrict__ active,
+    int tail_cap, int vecs, int* overflow) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int b = blockIdx.x;
+  if (active && active[b] == 0) return;
+  const int len = tail_len[b];   // every thread reads it before thread 0 advances it
+  if (len < 0 || len >= tail_cap) {
+    if (threadIdx.x == 0 && overflow) atomicOr(overflow, 1);
+    return;
+  }
+  const long long dst = (static_cast<long long>(b) * tail_cap + len) * vecs;
+  for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
+    k_tail[dst + i] = k_new[static_cast<long long>(b) * vecs + i];
+    v_tail[dst + i] = v_new[static_cast<long long>(b) * vecs + i];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) tail_len[b] = len + 1;
+}
+
 __global__ void __launch_bounds__(kThreads) unpack_tiles_kernel(
     const uint8_t* __restrict__ k_tiles, const uint8_t* __restrict__ v_tiles, uint4* __restrict__ k_dst,
     uint4* __restrict__ v_dst, int layer, int tok0, int n, int Hkv, int D, int T) {
@@ -130,6 +153,18 @@ cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst,
                                  dim3(kThreads), 0, s, static_cast<const uint4*>(k_src),
                                  static_cast<const uint4*>(v_src), static_cast<uint8_t*>(k_dst),
                                  static_cast<uint8_t*>(v_dst), L, n, Hkv, D, T, tok0, st, F, N);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_tail_append(void* k_tail, void* v_tail, int* tail_len, const void* k_new,
+                               const void* v_new, const int* active, int B, int tail_cap, int Hkv,
+                               int D, int* overflow, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  const int vecs = Hkv * D / 8;
+  const cudaError_t e = launch_k(tail_append_kernel, dim3(B), dim3(64), 0, s,
+                                 static_cast<uint4*>(k_tail), static_cast<uint4*>(v_tail), tail_len,
+                                 static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                                 active, tail_cap, vecs, overflow);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -340,9 +340,121 @@ rx_status rx_attend_suffix(rx_cache_t h, int layer, const void* q, const void* k
   if (!aligned16(q) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out))
     return fail(RX_ERR_ARG, "rx_attend_suffix: pointers must be 16-byte aligned");
   const rx::AttnLaunch a = make_launch(h, layer);
-  rx::AttnSegment seg{q, k_dyn, v_dyn, out, S, S, nullptr, 1, 0};
+  rx::AttnSegment seg{q, k_dyn, v_dyn, out, S, S, nullptr, 1, 0, 0};
   cudaError_t e = rx::launch_partitioned_attention(a, &seg, 1, static_cast<cudaStream_t>(stream), nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "rx_attend_suffix: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_attend_suffix_block_causal(rx_cache_t h, int layer, const void* q, const void* k_dyn,
+                                        const void* v_dyn, int S, int n_state, void* out,
+                                        void* stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_attend_suffix_block_causal: null cache");
+  const rx_config& c = h->cfg;
+  if (layer < 0 || layer >= c.L)
+    return fail(RX_ERR_LAYER, "rx_attend_suffix_block_causal: layer %d not in [0, %d)", layer, c.L);
+  if (S < 1) return fail(RX_ERR_ARG, "rx_attend_suffix_block_causal: S < 1");
+  if (S > c.S_cap) return fail(RX_ERR_CAPACITY, "rx_attend_suffix_block_causal: S = %d > S_cap = %d", S, c.S_cap);
+  if (n_state < 0 || n_state > S) return fail(RX_ERR_ARG, "rx_attend_suffix_block_causal: n_state = %d not in [0, S]", n_state);
+  if (!q || !k_dyn || !v_dyn || !out) return fail(RX_ERR_ARG, "rx_attend_suffix_block_causal: null pointer");
+  if (!aligned16(q) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out))
+    return fail(RX_ERR_ARG, "rx_attend_suffix_block_causal: pointers must be 16-byte aligned");
+  const rx::AttnLaunch a = make_launch(h, layer);
+  // n_state == S: every token is in the state block, which sees all S keys: plain Eq. 1.
+  rx::AttnSegment seg{q, k_dyn, v_dyn, out, S, S, nullptr, 1, 0, n_state < S ? n_state : 0};
+  cudaError_t e = rx::launch_partitioned_attention(a, &seg, 1, static_cast<cudaStream_t>(stream), nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_attend_suffix_block_causal: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_tail_append(void* k_tail, void* v_tail, int* tail_len, const void* k_new,
+                         const void* v_new, const int* active, int B, int tail_cap, int Hkv, int D,
+                         int* overflow, void* stream) {
+  RX_GUARD_BEGIN
+  if (B < 0 || tail_cap < 1 || Hkv < 1 || D < 1 || (static_cast<long long>(Hkv) * D) % 8)
+    return fail(RX_ERR_ARG, "rx_tail_append: sizes out of range (Hkv*D must be a multiple of 8)");
+  if (B == 0) return RX_OK;
+  if (!k_tail || !v_tail || !tail_len || !k_new || !v_new)
+    return fail(RX_ERR_ARG, "rx_tail_append: null pointer");
+  if (!aligned16(k_tail) || !aligned16(v_tail) || !aligned16(k_new) || !aligned16(v_new) ||
+      (reinterpret_cast<uintptr_t>(tail_len) & 3) || (reinterpret_cast<uintptr_t>(active) & 3) ||
+      (reinterpret_cast<uintptr_t>(overflow) & 3))
+    return fail(RX_ERR_ARG, "rx_tail_append: misaligned pointer");
+  cudaError_t e = rx::launch_tail_append(k_tail, v_tail, tail_len, k_new, v_new, active, B, tail_cap,
+                                         Hkv, D, overflow, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rx_tail_append: launch");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+namespace {
+// Snapshot layout: [SnapHeader, 256 B][pinned K | pinned V | window K | window V | DevState].
+struct SnapHeader {
+  char magic[8];
+  rx_config cfg;
+  int P;
+  long long host_pushes;
+  long long body_bytes;
+};
+static_assert(sizeof(SnapHeader) <= 256, "snapshot header");
+constexpr long long kSnapHeader = 256;
+
+long long snapshot_body(rx_cache_t h) {
+  return reinterpret_cast<const char*>(h->dstate) + sizeof(rx::DevState) -
+         reinterpret_cast<const char*>(h->k_pin);
+}
+}  // namespace
+
+rx_status rx_snapshot_bytes(rx_cache_t h, long long* bytes) {
+  RX_GUARD_BEGIN
+  if (!h || !bytes) return fail(RX_ERR_ARG, "rx_snapshot_bytes: null argument");
+  *bytes = kSnapHeader + snapshot_body(h);
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_snapshot(rx_cache_t h, void* dst, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h || !dst) return fail(RX_ERR_ARG, "rx_snapshot: null argument");
+  if (!aligned16(dst)) return fail(RX_ERR_ARG, "rx_snapshot: dst must be 16-byte aligned");
+  SnapHeader hd;
+  memset(&hd, 0, sizeof(hd));
+  memcpy(hd.magic, "RXSNAP01", 8);
+  hd.cfg = h->cfg;
+  hd.P = h->P;
+  hd.host_pushes = h->host_pushes;
+  hd.body_bytes = snapshot_body(h);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The header is staged from pageable memory before the call returns.
+  cudaError_t e = cudaMemcpyAsync(dst, &hd, sizeof(hd), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(static_cast<char*>(dst) + kSnapHeader, h->k_pin, hd.body_bytes,
+                        cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_snapshot: copy");
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_restore(rx_cache_t h, const void* src, void* stream) {
+  RX_GUARD_BEGIN
+  if (!h || !src) return fail(RX_ERR_ARG, "rx_restore: null argument");
+  if (!aligned16(src)) return fail(RX_ERR_ARG, "rx_restore: src must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SnapHeader hd;
+  cudaError_t e = cudaMemcpyAsync(&hd, src, sizeof(hd), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_restore: reading the header");
+  if (memcmp(hd.magic, "RXSNAP01", 8) != 0 || memcmp(&hd.cfg, &h->cfg, sizeof(rx_config)) != 0 ||
+      hd.body_bytes != snapshot_body(h))
+    return fail(RX_ERR_ARG, "rx_restore: not a snapshot of a cache with this configuration");
+  e = cudaMemcpyAsync(h->k_pin, static_cast<const char*>(src) + kSnapHeader, hd.body_bytes,
+                      cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_restore: copy");
+  h->P = hd.P;
+  h->host_pushes = hd.host_pushes;
   return RX_OK;
   RX_GUARD_END
 }
@@ -362,7 +474,7 @@ rx_status rx_attend_batch(rx_cache_t h, int layer, const void* q_act, const void
     if (!q_act || !k_dyn || !v_dyn || !out_act) return fail(RX_ERR_ARG, "rx_attend_batch: null action pointer");
     if (!aligned16(q_act) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out_act))
       return fail(RX_ERR_ARG, "rx_attend_batch: action pointers must be 16-byte aligned");
-    segs[nseg++] = rx::AttnSegment{q_act, k_dyn, v_dyn, out_act, S, S, nullptr, 1, 0};
+    segs[nseg++] = rx::AttnSegment{q_act, k_dyn, v_dyn, out_act, S, S, nullptr, 1, 0, 0};
   }
   if (lang && lang->B > 0) {
     const rx_stream_batch& b = *lang;
@@ -377,7 +489,7 @@ rx_status rx_attend_batch(rx_cache_t h, int layer, const void* q_act, const void
         (reinterpret_cast<uintptr_t>(b.tail_len) & 3))
       return fail(RX_ERR_ARG, "rx_attend_batch: language pointers misaligned");
     segs[nseg++] = rx::AttnSegment{b.q, b.k_tail, b.v_tail, b.out, b.B * b.T, b.B * c.tail_cap,
-                                   b.tail_len, b.T, c.tail_cap};
+                                   b.tail_len, b.T, c.tail_cap, 0};
   }
   if (nseg == 0) return RX_OK;
   const rx::AttnLaunch a = make_launch(h, layer);

@@ -77,6 +77,11 @@ cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst,
                               int L, int n, int Hkv, int D, int T, int tok0, DevState* st,
                               int F, int N, int num_sms, cudaStream_t s);
 
+// Append one token per active stream at tail_len[b] (bounded by tail_cap).
+cudaError_t launch_tail_append(void* k_tail, void* v_tail, int* tail_len, const void* k_new,
+                               const void* v_new, const int* active, int B, int tail_cap,
+                               int Hkv, int D, int* overflow, cudaStream_t s);
+
 // Inverse of the packing for one layer and token range (test aid):
 // dst [n][Hkv][D] <- tiles.
 cudaError_t launch_unpack_tiles(const void* k_tiles, const void* v_tiles, void* k_dst, void* v_dst,
@@ -132,6 +137,9 @@ struct AttnSegment {
   const int* tail_len;
   int tok_per_stream;
   int tail_cap;
+  // Block-causal suffix: tokens t < state_tokens see only private keys
+  // [0, state_tokens).  0 disables it.
+  int state_tokens;
 };
 
 // Launch the attention kernel over one or two segments (plus the split merge

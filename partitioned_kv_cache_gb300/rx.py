@@ -29,7 +29,8 @@ EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_fram
            "rx_attend_suffix", "rx_attend_batch", "rx_ada_gamma", "rx_adarmsnorm",
            "rx_get_state", "rx_debug_window", "rx_export_window", "rx_check_device_error",
            "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
-           "rx_attend_regions_static")
+           "rx_attend_regions_static", "rx_attend_suffix_block_causal", "rx_tail_append",
+           "rx_snapshot_bytes", "rx_snapshot", "rx_restore")
 
 
 class RxConfig(ctypes.Structure):
@@ -64,6 +65,11 @@ _sigs = {
     "rx_last_error": (ctypes.c_char_p, []),
     "rx_attend_regions_static": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _i,
                                       _vp, _vp, _i, _vp, _vp]),
+    "rx_attend_suffix_block_causal": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _vp, _vp]),
+    "rx_tail_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
+    "rx_snapshot_bytes": (_i, [_vp, ctypes.POINTER(ctypes.c_longlong)]),
+    "rx_snapshot": (_i, [_vp, _vp, _vp]),
+    "rx_restore": (_i, [_vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -147,14 +153,37 @@ class Cache:
         return ev.value
 
     def attend_suffix(self, layer: int, q: torch.Tensor, k_dyn: torch.Tensor, v_dyn: torch.Tensor,
-                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                      out: Optional[torch.Tensor] = None, stream=None,
+                      n_state: Optional[int] = None) -> torch.Tensor:
+        """Eq. 1 for one layer; with n_state, the block-causal variant (the
+        first n_state suffix tokens see only their own dynamic keys)."""
         S = q.shape[0]
         if out is None:
             out = torch.empty_like(q)
-        _check(_lib.rx_attend_suffix(self._h, layer, _ptr(q, name="q"), _ptr(k_dyn, name="k_dyn"),
-                                     _ptr(v_dyn, name="v_dyn"), S, _ptr(out, name="out"),
-                                     _stream(stream)), "rx_attend_suffix")
+        if n_state is None:
+            _check(_lib.rx_attend_suffix(self._h, layer, _ptr(q, name="q"), _ptr(k_dyn, name="k_dyn"),
+                                         _ptr(v_dyn, name="v_dyn"), S, _ptr(out, name="out"),
+                                         _stream(stream)), "rx_attend_suffix")
+        else:
+            _check(_lib.rx_attend_suffix_block_causal(
+                self._h, layer, _ptr(q, name="q"), _ptr(k_dyn, name="k_dyn"), _ptr(v_dyn, name="v_dyn"),
+                S, int(n_state), _ptr(out, name="out"), _stream(stream)), "rx_attend_suffix_block_causal")
         return out
+
+    def snapshot_bytes(self) -> int:
+        n = ctypes.c_longlong(0)
+        _check(_lib.rx_snapshot_bytes(self._h, ctypes.byref(n)), "rx_snapshot_bytes")
+        return n.value
+
+    def snapshot(self, dst: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """Copy the cache's state into a uint8 CUDA tensor (allocated if not given)."""
+        if dst is None:
+            dst = torch.empty(self.snapshot_bytes(), dtype=torch.uint8, device="cuda")
+        _check(_lib.rx_snapshot(self._h, _ptr(dst, torch.uint8, "dst"), _stream(stream)), "rx_snapshot")
+        return dst
+
+    def restore(self, src: torch.Tensor, stream=None) -> None:
+        _check(_lib.rx_restore(self._h, _ptr(src, torch.uint8, "src"), _stream(stream)), "rx_restore")
 
     def attend_batch(self, layer: int, action=None, lang=None, out_act: Optional[torch.Tensor] = None,
                      out_lang: Optional[torch.Tensor] = None, stream=None):
@@ -270,3 +299,16 @@ def attend_regions_static(q: torch.Tensor, k_pin: Optional[torch.Tensor], v_pin:
                                          _ptr(out, name="out"), _stream(stream)),
            "rx_attend_regions_static")
     return out
+
+
+def tail_append(k_tail: torch.Tensor, v_tail: torch.Tensor, tail_len: torch.Tensor,
+                k_new: torch.Tensor, v_new: torch.Tensor, active: Optional[torch.Tensor] = None,
+                overflow: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Append one token per (active) stream: tails [B][tail_cap][Hkv][D],
+    tail_len int32 [B] (advanced on the device), new tokens [B][Hkv][D]."""
+    B, tail_cap, Hkv, D = k_tail.shape
+    _check(_lib.rx_tail_append(_ptr(k_tail, name="k_tail"), _ptr(v_tail, name="v_tail"),
+                               _ptr(tail_len, torch.int32, "tail_len"), _ptr(k_new, name="k_new"),
+                               _ptr(v_new, name="v_new"), _ptr(active, torch.int32, "active"), B,
+                               tail_cap, Hkv, D, _ptr(overflow, torch.int32, "overflow"),
+                               _stream(stream)), "rx_tail_append")

@@ -150,3 +150,31 @@ def test_c4_outliers_present():
     a = np.abs(W.bf16_bits_to_f64(k))
     frac = float(np.mean(a > 8.0))
     assert 0.004 < frac < 0.012
+
+
+def test_block_causal_reduces_to_eq1_and_matches_masked_sdpa():
+    """n_state = 0 (and n_state = S) is plain Eq. 1; otherwise it equals torch
+    SDPA with the explicit boolean mask, and a brute-force masked loop."""
+    q = _randn(40, 6, 2, 8)
+    regions = [(_randn(41, 5, 1, 8), _randn(42, 5, 1, 8)), (_randn(43, 7, 1, 8), _randn(44, 7, 1, 8)),
+               (_randn(45, 6, 1, 8), _randn(46, 6, 1, 8))]
+    ks, vs = [r[0] for r in regions], [r[1] for r in regions]
+    full = A.partitioned_attention(q, ks, vs)
+    np.testing.assert_allclose(A.block_causal_attention(q, ks, vs, 0), full, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(A.block_causal_attention(q, ks, vs, 6), full, rtol=0, atol=1e-15)
+    n_state = 2
+    got = A.block_causal_attention(q, ks, vs, n_state)
+    K, V = np.concatenate(ks), np.concatenate(vs)
+    T, cached = K.shape[0], 12
+    allowed = np.ones((6, T), dtype=bool)
+    allowed[:n_state, cached + n_state:] = False
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    kt = torch.from_numpy(K).permute(1, 0, 2).expand(2, -1, -1)
+    vt = torch.from_numpy(V).permute(1, 0, 2).expand(2, -1, -1)
+    ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(allowed)).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    # brute force on the state rows: drop the masked keys explicitly
+    keep = [j for j in range(T) if allowed[0, j]]
+    bf = np.array(A.brute_force_attention(q[:n_state].tolist(), K[keep].tolist(), V[keep].tolist()))
+    np.testing.assert_allclose(got[:n_state], bf, rtol=0, atol=1e-12)
+    assert np.max(np.abs(got[:n_state] - full[:n_state])) > 1e-3
