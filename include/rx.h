@@ -79,6 +79,9 @@ typedef struct rx_config {
   int S_cap;    /* most query tokens of one attention call (>= 1)           */
   int tail_cap; /* private tail capacity of a language stream (>= 0)        */
   int max_req;  /* most language query tokens (B*T) of one rx_attend_batch  */
+  int spare_slot; /* 1: keep one spare frame slot (N+1 slots) so that pushes
+                     can run concurrently with attention (rx_push_frame_async);
+                     requires F % 64 == 0.  0: N slots.                      */
 } rx_config;
 
 /* Allocate and zero every region ("Reflex ...", §V: the ring buffer is
@@ -110,6 +113,24 @@ rx_status rx_pin_prefix(rx_cache_t cache, const void* k, const void* v, int P,
  * Errors: RX_ERR_ARG, RX_ERR_CUDA. */
 rx_status rx_push_frame(rx_cache_t cache, const void* k, const void* v,
                         int* evicted, void* stream);
+
+/* Ring append on a producer stream, concurrent with attention on a consumer
+ * stream ("Reflex ...", §III "System architecture": Thread A encodes frames
+ * into the ring buffer while Thread B reads the latest tokens and denoises).
+ * Needs a cache created with spare_slot = 1.  The frame is written into the
+ * spare slot, which no published window contains; the last CTA then
+ * publishes {head, valid} in one 64-bit store, so an attention kernel reads
+ * either the previous window or the new one, never a mix.  Ordering, by CUDA
+ * events (no device spinning): producer_stream first waits for all work
+ * already enqueued on consumer_stream, and consumer_stream waits for the
+ * previous asynchronous push.  So every attention enqueued after this call sees
+ * the window after the previous push or after this one, and the slot this push
+ * overwrites can only be read by work that the producer waited for.  The push
+ * runs concurrently with consumer work enqueued after the call.
+ * Errors: RX_ERR_STATE (cache without a spare slot), RX_ERR_ARG, RX_ERR_CUDA. */
+rx_status rx_push_frame_async(rx_cache_t cache, const void* k, const void* v,
+                              int* evicted, void* producer_stream,
+                              void* consumer_stream);
 
 /* Partitioned attention for one layer ("Reflex ...", §III Eq. 1): for every
  * suffix token s and query head h,

@@ -146,6 +146,7 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
     a.P = P;
     a.F = 1;
     a.N = W;
+    a.slots = W;
     a.D = D;
     a.Hq = Hq;
     a.Hkv = Hkv;

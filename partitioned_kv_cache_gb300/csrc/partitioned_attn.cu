@@ -110,7 +110,7 @@ struct AttnParams {
   const DevState* st;
   int* err;
   int layer;
-  int P, F;
+  int P, F, N, slots;    // pinned tokens; window: tokens per frame, frames, frame slots
   int Hq, G;
   int rows_pad;          // workspace rows of all segments
   int n_splits;
@@ -120,24 +120,31 @@ struct AttnParams {
 
 struct TileInfo {
   int region;   // 0 pinned, 1 window, 2 dynamic
-  int key0;     // first key of the tile within its region
+  int key0;     // first key of the tile among the region's keys (masks, stream windows)
+  int phys0;    // first stored token of the tile (where it is read from)
   int nvalid;   // keys of the tile inside the region (1..64)
 };
 
+// Window tiles skip the spare slot's tiles [hole0, hole0 + hole_n) once the
+// ring is full (hole_n = 0 otherwise).
 __device__ __forceinline__ TileInfo tile_at(int t, int nt_pin, int nt_win, int P, int win_len,
-                                            int n_priv) {
+                                            int n_priv, int hole0, int hole_n) {
   TileInfo ti;
   if (t < nt_pin) {
     ti.region = 0;
     ti.key0 = t * kBN;
+    ti.phys0 = ti.key0;
     ti.nvalid = min(kBN, P - ti.key0);
   } else if (t < nt_pin + nt_win) {
+    const int tw = t - nt_pin;
     ti.region = 1;
-    ti.key0 = (t - nt_pin) * kBN;
+    ti.key0 = tw * kBN;
+    ti.phys0 = (tw < hole0 ? tw : tw + hole_n) * kBN;
     ti.nvalid = min(kBN, win_len - ti.key0);
   } else {
     ti.region = 2;
     ti.key0 = (t - nt_pin - nt_win) * kBN;
+    ti.phys0 = ti.key0;
     ti.nvalid = min(kBN, n_priv - ti.key0);
   }
   return ti;
@@ -268,10 +275,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   // here on the kernel reads inputs an earlier kernel may have written.
   grid_dependency_wait();
   grid_launch_dependents();
-  // Key tiles of this split.  The window length comes from the device-side
-  // ring state written by the append kernel earlier in stream order.
-  const int valid = *reinterpret_cast<const volatile int*>(&p.st->valid);
-  const int win_len = valid * p.F;
+  // Key tiles of this split.  The window comes from the device-side ring state
+  // published by the append kernel (one 64-bit word: a consistent snapshot
+  // even while a push on another stream is publishing).
+  int head = 0, valid = 0;
+  load_ring_state(p.st, &head, &valid);
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");   // frame data before the snapshot
+  // With a spare slot and a full ring the window is every slot but `head`.
+  const bool hole = p.slots > p.N && valid == p.N;
+  const int win_len = hole ? (p.slots - 1) * p.F : valid * p.F;
+  const int hole0 = hole ? head * p.F / kBN : 0;
+  const int hole_n = hole ? p.F / kBN : 0;
   const int nt_pin = (p.P + kBN - 1) / kBN;
   const int nt_win = (win_len + kBN - 1) / kBN;
   const int nt_dyn = (sg.n_priv + kBN - 1) / kBN;
@@ -295,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       for (int kb = 0; kb < Lay::KB; ++kb)
         tma_load_4d(sQ + kb * Lay::Q_BLOCK, &sg.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
       for (int j = 0; j < n && issued >= 0; ++j) {
-        const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv);
+        const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv, hole0, hole_n);
         const int lay = ti.region == 2 ? 0 : p.layer;
         for (int kv = 0; kv < 2; ++kv) {
           const int it = issued;
@@ -308,13 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           mbar_arrive_expect_tx(BAR(B_FULL + slot), Lay::TILE);
           const uint8_t* tiles = ti.region < 2 ? (kv ? p.v_tiles[ti.region] : p.k_tiles[ti.region]) : nullptr;
           if (tiles) {
-            bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.key0 / kBN) * Lay::TILE,
+            bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE,
                       Lay::TILE, BAR(B_FULL + slot));
           } else {
             const CUtensorMap* tm = ti.region == 2 ? (kv ? &sg.tm_vp : &sg.tm_kp)
                                                    : (kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region]);
             for (int kb = 0; kb < Lay::KB; ++kb)
-              tma_load_4d(dst + kb * 8192, tm, kb * 64, g, ti.key0, lay, BAR(B_FULL + slot));
+              tma_load_4d(dst + kb * 8192, tm, kb * 64, g, ti.phys0, lay, BAR(B_FULL + slot));
           }
           issued = it + 1;
         }
@@ -418,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       float s[kBN];
       tmem_ld32(tS + st * kBN + lane_off, s);
       tmem_ld32(tS + st * kBN + 32 + lane_off, s + 32);
-      const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv);
+      const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv, hole0, hole_n);
       if (ti.region == 2 && priv_masked) {   // private keys outside this row's window
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
@@ -847,6 +861,8 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   prm.layer = a.layer;
   prm.P = a.P;
   prm.F = a.F;
+  prm.N = a.N;
+  prm.slots = a.slots > 0 ? a.slots : a.N;
   prm.Hq = a.Hq;
   prm.G = G;
   prm.rows_pad = m_total * kBM;

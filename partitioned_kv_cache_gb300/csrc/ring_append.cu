@@ -6,10 +6,12 @@
 // §V "Key implementation": add_new_prefix() adds the new tokens and reports
 // evictions, evict_source_prefix() drops the oldest frame from all layers.
 //
-// The window of (layer l, K/V head g) holds N frame slots of F tokens; slot s
-// covers window tokens [s*F, s*F + F).  A push writes the frame into slot
-// `head` of every layer -- overwriting the oldest frame once the window is
-// full, which is the eviction -- and advances head <- (head+1) mod N,
+// The window of (layer l, K/V head g) holds N frame slots of F tokens (N + 1
+// with a spare slot); slot s covers window tokens [s*F, s*F + F).  A push
+// writes the frame into slot `head` of every layer -- overwriting the oldest
+// frame once the window is full, which is the eviction (with a spare slot the
+// overwritten slot is the one evicted by the previous push, already outside
+// every published window) -- and advances head <- (head+1) mod slots,
 // valid <- min(valid+1, N).  Nothing else moves.  The state update is done on
 // the device by the last CTA to finish, so a captured CUDA graph replays
 // pushes correctly.
@@ -42,12 +44,13 @@ __device__ __forceinline__ long long tiled_offset(int l, int g, int Hkv, int T, 
 __global__ void __launch_bounds__(kThreads) pack_tiles_kernel(
     const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint8_t* __restrict__ k_dst,
     uint8_t* __restrict__ v_dst, int L, int n, int Hkv, int D, int T, int tok0, DevState* st,
-    int F, int N) {
+    int F, int N, int slots) {
   grid_dependency_wait();
   grid_launch_dependents();
-  // A ring append reads head before any CTA can update it (the update waits
-  // for every CTA to arrive).
-  const int head = st ? *reinterpret_cast<volatile int*>(&st->head) : 0;
+  // A ring append reads the state before any CTA can update it (the update
+  // waits for every CTA to arrive).
+  int head = 0, valid = 0;
+  if (st) load_ring_state(st, &head, &valid);
   const int base_tok = st ? head * F : tok0;
   const int cpt = D >> 3;   // 16-byte chunks per token and head
   const long long total = static_cast<long long>(L) * n * Hkv * cpt;
@@ -86,8 +89,9 @@ __global__ void __launch_bounds__(kThreads) pack_tiles_kernel(
     __threadfence();
     const unsigned int prev = atomicAdd(&st->append_arrivals, 1u);
     if (prev == gridDim.x - 1) {
-      st->head = head + 1 == N ? 0 : head + 1;
-      st->valid = st->valid < N ? st->valid + 1 : N;
+      // Every CTA fenced its frame writes before arriving: publish.
+      __threadfence();
+      publish_ring_state(st, head + 1 == slots ? 0 : head + 1, valid < N ? valid + 1 : N);
       st->pushes += 1;
       st->append_arrivals = 0;
       __threadfence();
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) unpack_tiles_kernel(
 
 cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
                               int L, int n, int Hkv, int D, int T, int tok0, DevState* st, int F,
-                              int N, int num_sms, cudaStream_t s) {
+                              int N, int slots, int num_sms, cudaStream_t s) {
   const long long total = static_cast<long long>(L) * n * Hkv * (D >> 3);
   long long blocks = (total + static_cast<long long>(kThreads) * kVecPerThread - 1) /
                      (static_cast<long long>(kThreads) * kVecPerThread);
@@ -152,7 +156,7 @@ cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst,
   const cudaError_t e = launch_k(pack_tiles_kernel, dim3(static_cast<unsigned int>(blocks)),
                                  dim3(kThreads), 0, s, static_cast<const uint4*>(k_src),
                                  static_cast<const uint4*>(v_src), static_cast<uint8_t*>(k_dst),
-                                 static_cast<uint8_t*>(v_dst), L, n, Hkv, D, T, tok0, st, F, N);
+                                 static_cast<uint8_t*>(v_dst), L, n, Hkv, D, T, tok0, st, F, N, slots);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

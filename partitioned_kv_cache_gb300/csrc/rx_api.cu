@@ -123,6 +123,10 @@ struct rx_cache {
   int max_splits = 0;
   int T_pin = 0;         // tiles of the pinned region per (layer, head), >= 1
   int T_win = 0;         // tiles of the window per (layer, head)
+  int slots = 0;         // frame slots of the window: N, or N + 1 with a spare slot
+  cudaEvent_t consumer_done = nullptr;   // rx_push_frame_async ordering: consumer work so far
+  cudaEvent_t push_done = nullptr;       // ... and the previous asynchronous push
+  long long async_pushes = 0;
   int P = 0;             // pinned tokens currently held
   long long host_pushes = 0;
   int forced_splits = 0;
@@ -167,6 +171,9 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
       c.tail_cap < 0 || c.max_req < 0)
     return fail(RX_ERR_ARG, "rx_cache_create: sizes out of range");
   if (c.Hq % c.Hkv) return fail(RX_ERR_ARG, "rx_cache_create: Hq must be a multiple of Hkv");
+  if (c.spare_slot != 0 && c.spare_slot != 1) return fail(RX_ERR_ARG, "rx_cache_create: spare_slot must be 0 or 1");
+  if (c.spare_slot && c.F % rx::kTileTok)
+    return fail(RX_ERR_UNSUPPORTED, "rx_cache_create: a spare slot needs F %% 64 == 0 (F = %d)", c.F);
   const int G = c.Hq / c.Hkv;
   if (!pow2(G) || G > rx::kBM)
     return fail(RX_ERR_UNSUPPORTED, "rx_cache_create: Hq/Hkv = %d must be a power of two <= 128", G);
@@ -188,7 +195,8 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   h->num_sms = prop.multiProcessorCount;
   h->max_splits = h->num_sms < 64 ? h->num_sms : 64;
   h->T_pin = rx::tiles_for(c.P_cap > 0 ? c.P_cap : 1);
-  h->T_win = rx::tiles_for(static_cast<long long>(c.N) * c.F);
+  h->slots = c.N + c.spare_slot;
+  h->T_win = rx::tiles_for(static_cast<long long>(h->slots) * c.F);
 
   const size_t tile = static_cast<size_t>(rx::tile_bytes(c.D));
   const size_t pin_b = round_up(static_cast<size_t>(c.L) * c.Hkv * h->T_pin * tile, 256);
@@ -221,6 +229,15 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   h->dstate = reinterpret_cast<rx::DevState*>(p); p += st_b;
   h->part_o = reinterpret_cast<float*>(p); p += po_b;
   h->part_ml = reinterpret_cast<float2*>(p);
+  if (c.spare_slot) {
+    e = cudaEventCreateWithFlags(&h->consumer_done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->push_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      cudaFree(h->mem);
+      delete h;
+      return cuda_fail(e, "rx_cache_create: cudaEventCreate");
+    }
+  }
   *out = h;
   return RX_OK;
   RX_GUARD_END
@@ -230,6 +247,8 @@ rx_status rx_cache_destroy(rx_cache_t h) {
   RX_GUARD_BEGIN
   if (!h) return RX_OK;
   cudaError_t e = cudaDeviceSynchronize();
+  if (h->consumer_done) cudaEventDestroy(h->consumer_done);
+  if (h->push_done) cudaEventDestroy(h->push_done);
   cudaError_t e2 = cudaFree(h->mem);
   delete h;
   if (e != cudaSuccess) return cuda_fail(e, "rx_cache_destroy: synchronize");
@@ -270,7 +289,7 @@ rx_status rx_pin_prefix(rx_cache_t h, const void* k, const void* v, int P, void*
     }
     if (e == cudaSuccess)
       e = rx::launch_pack_tiles(sk, sv, h->k_pin, h->v_pin, c.L, P, c.Hkv, c.D, h->T_pin, 0, nullptr,
-                                0, 0, h->num_sms, s);
+                                0, 0, 0, h->num_sms, s);
     if (tmp) {
       const cudaError_t e2 = cudaStreamSynchronize(s);
       cudaFree(tmp);
@@ -290,11 +309,40 @@ rx_status rx_push_frame(rx_cache_t h, const void* k, const void* v, int* evicted
   if (!aligned16(k) || !aligned16(v)) return fail(RX_ERR_ARG, "rx_push_frame: K/V not 16-byte aligned");
   const rx_config& c = h->cfg;
   cudaError_t e = rx::launch_pack_tiles(k, v, h->k_win, h->v_win, c.L, c.F, c.Hkv, c.D, h->T_win, 0,
-                                        h->dstate, c.F, c.N, h->num_sms,
+                                        h->dstate, c.F, c.N, h->slots, h->num_sms,
                                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rx_push_frame: launch");
   if (evicted) *evicted = h->host_pushes >= c.N ? 1 : 0;
   h->host_pushes += 1;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_push_frame_async(rx_cache_t h, const void* k, const void* v, int* evicted,
+                              void* producer_stream, void* consumer_stream) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_push_frame_async: null cache");
+  if (!h->cfg.spare_slot) return fail(RX_ERR_STATE, "rx_push_frame_async: the cache has no spare slot");
+  if (!k || !v) return fail(RX_ERR_ARG, "rx_push_frame_async: null K/V");
+  if (!aligned16(k) || !aligned16(v)) return fail(RX_ERR_ARG, "rx_push_frame_async: K/V not 16-byte aligned");
+  const rx_config& c = h->cfg;
+  cudaStream_t ps = static_cast<cudaStream_t>(producer_stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(consumer_stream);
+  // This push overwrites the slot the previous push evicted.  Windows that
+  // contain it were published before the previous push; work enqueued on the
+  // consumer stream from now on waits for the previous push, so only work
+  // already enqueued may still read the slot: the producer waits for that.
+  cudaError_t e = cudaEventRecord(h->consumer_done, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ps, h->consumer_done, 0);
+  if (e == cudaSuccess && h->async_pushes > 0) e = cudaStreamWaitEvent(cs, h->push_done, 0);
+  if (e == cudaSuccess)
+    e = rx::launch_pack_tiles(k, v, h->k_win, h->v_win, c.L, c.F, c.Hkv, c.D, h->T_win, 0, h->dstate,
+                              c.F, c.N, h->slots, h->num_sms, ps);
+  if (e == cudaSuccess) e = cudaEventRecord(h->push_done, ps);
+  if (e != cudaSuccess) return cuda_fail(e, "rx_push_frame_async");
+  if (evicted) *evicted = h->host_pushes >= c.N ? 1 : 0;
+  h->host_pushes += 1;
+  h->async_pushes += 1;
   return RX_OK;
   RX_GUARD_END
 }
@@ -315,6 +363,7 @@ static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   a.P = h->P;
   a.F = h->cfg.F;
   a.N = h->cfg.N;
+  a.slots = h->slots;
   a.D = h->cfg.D;
   a.Hq = h->cfg.Hq;
   a.Hkv = h->cfg.Hkv;
@@ -573,9 +622,9 @@ rx_status rx_debug_window(rx_cache_t h, int* slots, int* valid, void* stream) {
   rx::DevState ds;
   rx_status r = read_state(h, &ds, static_cast<cudaStream_t>(stream));
   if (r != RX_OK) return r;
-  const int N = h->cfg.N;
-  const int oldest = ((ds.head - ds.valid) % N + N) % N;
-  for (int i = 0; i < ds.valid; ++i) slots[i] = (oldest + i) % N;
+  const int ns = h->slots;
+  const int oldest = ((ds.head - ds.valid) % ns + ns) % ns;
+  for (int i = 0; i < ds.valid; ++i) slots[i] = (oldest + i) % ns;
   *valid = ds.valid;
   return RX_OK;
   RX_GUARD_END

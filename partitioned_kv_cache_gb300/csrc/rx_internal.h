@@ -12,13 +12,27 @@ namespace rx {
 // Device-side ring state of one cache.  Lives in the cache's allocation and
 // is advanced by the append kernel itself, so captured graphs replay it.
 struct DevState {
-  int head;        // slot the next push writes
-  int valid;       // frames held, min(pushes, N)
+  // head (slot the next push writes) and valid (frames held, <= N) are one
+  // 64-bit word: the append publishes both with a single store and readers
+  // load both with a single load.
+  int head;
+  int valid;
   long long pushes;
   unsigned int append_arrivals;   // CTAs of the running append that finished
   int err;         // error bits set by kernels (see kErr*)
   int pad[2];
 };
+
+__device__ __forceinline__ void load_ring_state(const DevState* st, int* head, int* valid) {
+  const unsigned long long hv = *reinterpret_cast<const volatile unsigned long long*>(st);
+  *head = static_cast<int>(hv & 0xFFFFFFFFull);
+  *valid = static_cast<int>(hv >> 32);
+}
+__device__ __forceinline__ void publish_ring_state(DevState* st, int head, int valid) {
+  *reinterpret_cast<volatile unsigned long long*>(st) =
+      static_cast<unsigned long long>(static_cast<unsigned int>(head)) |
+      (static_cast<unsigned long long>(static_cast<unsigned int>(valid)) << 32);
+}
 
 constexpr int kErrAttnTimeout = 1;    // attention kernel: a bounded wait gave up
 constexpr int kErrBatchTimeout = 2;   // batched attention: a bounded wait gave up
@@ -75,7 +89,7 @@ __host__ __device__ constexpr int tiles_for(long long tokens) {
 // head * F read on the device, and the last CTA advances {head, valid}.
 cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
                               int L, int n, int Hkv, int D, int T, int tok0, DevState* st,
-                              int F, int N, int num_sms, cudaStream_t s);
+                              int F, int N, int slots, int num_sms, cudaStream_t s);
 
 // Append one token per active stream at tail_len[b] (bounded by tail_cap).
 cudaError_t launch_tail_append(void* k_tail, void* v_tail, int* tail_len, const void* k_new,
@@ -113,6 +127,7 @@ struct AttnLaunch {
   long long pin_head_stride;    // bytes between K/V heads of the tiled regions
   long long win_head_stride;
   int layer, P, F, N, D, Hq, Hkv;
+  int slots;          // frame slots of the window: N, or N + 1 with a spare slot
   const DevState* st;
   int* err;
   float* part_o;      // workspace: [Hkv][splits][D][tiles*128] fp32

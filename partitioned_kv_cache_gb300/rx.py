@@ -30,12 +30,13 @@ EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_fram
            "rx_get_state", "rx_debug_window", "rx_export_window", "rx_check_device_error",
            "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
            "rx_attend_regions_static", "rx_attend_suffix_block_causal", "rx_tail_append",
-           "rx_snapshot_bytes", "rx_snapshot", "rx_restore")
+           "rx_snapshot_bytes", "rx_snapshot", "rx_restore", "rx_push_frame_async")
 
 
 class RxConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("L", "Hq", "Hkv", "D", "P_cap", "N", "F", "S_cap", "tail_cap", "max_req")]
+                ("L", "Hq", "Hkv", "D", "P_cap", "N", "F", "S_cap", "tail_cap", "max_req",
+                 "spare_slot")]
 
 
 class RxStreamBatch(ctypes.Structure):
@@ -70,6 +71,7 @@ _sigs = {
     "rx_snapshot_bytes": (_i, [_vp, ctypes.POINTER(ctypes.c_longlong)]),
     "rx_snapshot": (_i, [_vp, _vp, _vp]),
     "rx_restore": (_i, [_vp, _vp, _vp]),
+    "rx_push_frame_async": (_i, [_vp, _vp, _vp, ctypes.POINTER(_i), _vp, _vp]),
 }
 for _name, (_res, _args) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -119,8 +121,8 @@ class Cache:
     """The partitioned KV store of one stream (rx_cache_t)."""
 
     def __init__(self, L: int, Hq: int, Hkv: int, D: int, P_cap: int, N: int, F: int,
-                 S_cap: int, tail_cap: int = 0, max_req: int = 0):
-        self.cfg = RxConfig(L, Hq, Hkv, D, P_cap, N, F, S_cap, tail_cap, max_req)
+                 S_cap: int, tail_cap: int = 0, max_req: int = 0, spare_slot: int = 0):
+        self.cfg = RxConfig(L, Hq, Hkv, D, P_cap, N, F, S_cap, tail_cap, max_req, spare_slot)
         h = _vp()
         _check(_lib.rx_cache_create(ctypes.byref(self.cfg), ctypes.byref(h)), "rx_cache_create")
         self._h = h
@@ -150,6 +152,16 @@ class Cache:
         ev = _i(0)
         _check(_lib.rx_push_frame(self._h, _ptr(k, name="k"), _ptr(v, name="v"),
                                   ctypes.byref(ev), _stream(stream)), "rx_push_frame")
+        return ev.value
+
+    def push_frame_async(self, k: torch.Tensor, v: torch.Tensor, producer_stream,
+                         consumer_stream) -> int:
+        """Push on producer_stream, concurrent with attention on consumer_stream
+        (needs spare_slot=1)."""
+        ev = _i(0)
+        _check(_lib.rx_push_frame_async(self._h, _ptr(k, name="k"), _ptr(v, name="v"), ctypes.byref(ev),
+                                        producer_stream.cuda_stream, consumer_stream.cuda_stream),
+               "rx_push_frame_async")
         return ev.value
 
     def attend_suffix(self, layer: int, q: torch.Tensor, k_dyn: torch.Tensor, v_dyn: torch.Tensor,

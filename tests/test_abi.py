@@ -46,12 +46,12 @@ def test_create_rejects_bad_configs_without_a_device(lib):
     from partitioned_kv_cache_gb300 import rx
     h = ctypes.c_void_p()
     bad = [
-        rx.RxConfig(0, 8, 1, 256, 64, 8, 256, 51, 0, 0),     # L = 0
-        rx.RxConfig(1, 8, 3, 256, 64, 8, 256, 51, 0, 0),     # Hq % Hkv
-        rx.RxConfig(1, 8, 1, 96, 64, 8, 256, 51, 0, 0),      # D
-        rx.RxConfig(1, 8, 1, 256, 64, 0, 256, 51, 0, 0),     # N = 0
-        rx.RxConfig(1, 8, 1, 256, -1, 8, 256, 51, 0, 0),     # P_cap < 0
-        rx.RxConfig(1, 6, 1, 256, 64, 8, 256, 51, 0, 0),     # G = 6 not a power of two
+        rx.RxConfig(0, 8, 1, 256, 64, 8, 256, 51, 0, 0, 0),     # L = 0
+        rx.RxConfig(1, 8, 3, 256, 64, 8, 256, 51, 0, 0, 0),     # Hq % Hkv
+        rx.RxConfig(1, 8, 1, 96, 64, 8, 256, 51, 0, 0, 0),      # D
+        rx.RxConfig(1, 8, 1, 256, 64, 0, 256, 51, 0, 0, 0),     # N = 0
+        rx.RxConfig(1, 8, 1, 256, -1, 8, 256, 51, 0, 0, 0),     # P_cap < 0
+        rx.RxConfig(1, 6, 1, 256, 64, 8, 256, 51, 0, 0, 0),     # G = 6 not a power of two
     ]
     for cfg in bad:
         st = rx._lib.rx_cache_create(ctypes.byref(cfg), ctypes.byref(h))
