@@ -25,12 +25,14 @@
 //     kept: exact after the final division by the row sum).
 //   * The key sequence is split across CTAs (gridDim.y).  When the splits of an
 //     M-tile form one thread-block cluster (up to kMaxClusterSplits), each CTA
-//     parks its fp32 (O, m, l) in its own shared memory and the cluster
-//     combines them through distributed shared memory, every CTA finishing a
-//     disjoint set of 32-column chunks of the bf16 output: no partials leave
-//     the chip and no second kernel runs.  Beyond that size each split writes
-//     an fp32 partial to global memory and a merge kernel combines them.  With
-//     a single split the CTA writes the bf16 output directly.
+//     parks its normalised partial O / l (bf16, in 16-column halves of 4 KB)
+//     and its fp32 (m, l) in its own shared memory, then pushes every half
+//     with one bulk copy to the cluster CTA that owns those columns; owners
+//     read all splits' (m, l) through distributed shared memory and finish
+//     their columns of the bf16 output: no partials leave the chip and no
+//     second kernel runs.  Beyond that size each split writes an fp32 partial
+//     to global memory and a merge kernel combines them.  With a single split
+//     the CTA writes the bf16 output directly.
 //
 // Warp roles (224 threads): warp 0 = copy producer, warp 1 = TMEM allocator and
 // Q K^T issuer, warp 6 = P V issuer, warps 2..5 = softmax and epilogue (TMEM

@@ -102,9 +102,13 @@ WORKLOADS: Dict[str, Workload] = {
 def to_bf16_bits(x) -> np.ndarray:
     """float -> bf16 bit pattern, round to nearest even (finite inputs)."""
     f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    u = f.view(np.uint32)
+    # u + 0x7FFF + lsb stays below 2^32 for every finite float32
+    r = (u >> 16) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:
