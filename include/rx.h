@@ -274,6 +274,13 @@ rx_status rx_check_device_error(rx_cache_t cache, int* code, void* stream);
  * the same for every value up to rounding order. */
 rx_status rx_set_attn_splits(rx_cache_t cache, int splits);
 
+/* Number of CTAs that share the output columns of one (query tile, split):
+ * each computes the scores in full but the value product, and the partial it
+ * merges, for D/dparts columns only.  1, 2 or 4 with D/dparts >= 64, or 0 =
+ * chosen from the SM count (the default).  A tuning knob: results are the
+ * same for every value up to rounding order.  Errors: RX_ERR_ARG. */
+rx_status rx_set_attn_dparts(rx_cache_t cache, int dparts);
+
 /* Kernel launches made by the library in this process (all entry points,
  * all caches).  For accounting in benchmarks. */
 long long rx_launch_count(void);

@@ -60,13 +60,23 @@ __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict
   uint4* yr = y + row * nv;
   const float inv_d = 1.0f / static_cast<float>(d);
   if constexpr (MAXV > 0) {
+    // The row and its gamma slice are loaded together, so the gamma read is
+    // not a second round trip after the reduction.
     uint4 xv[MAXV];
-    float ss = 0.f;
+    float4 g0[MAXV], g1[MAXV];
 #pragma unroll
     for (int u = 0; u < MAXV; ++u) {
       const int v = lane + 32 * u;
       if (v < nv) {
         xv[u] = xr[v];
+        g0[u] = *reinterpret_cast<const float4*>(gamma + 8 * v);
+        g1[u] = *reinterpret_cast<const float4*>(gamma + 8 * v + 4);
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u) {
+      if (lane + 32 * u < nv) {
         float f[8];
         unpack8(xv[u], f);
 #pragma unroll
@@ -80,12 +90,10 @@ __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict
       if (v < nv) {
         float f[8];
         unpack8(xv[u], f);
-        const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * v);
-        const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * v + 4);
-        yr[v] = make_uint4(pack2(f[0] * r * g0.x, f[1] * r * g0.y),
-                           pack2(f[2] * r * g0.z, f[3] * r * g0.w),
-                           pack2(f[4] * r * g1.x, f[5] * r * g1.y),
-                           pack2(f[6] * r * g1.z, f[7] * r * g1.w));
+        yr[v] = make_uint4(pack2(f[0] * r * g0[u].x, f[1] * r * g0[u].y),
+                           pack2(f[2] * r * g0[u].z, f[3] * r * g0[u].w),
+                           pack2(f[4] * r * g1[u].x, f[5] * r * g1[u].y),
+                           pack2(f[6] * r * g1[u].z, f[7] * r * g1[u].w));
       }
     }
   } else {

@@ -24,15 +24,14 @@
 //     running maximum grows by more than 2^8 (otherwise the stale maximum is
 //     kept: exact after the final division by the row sum).
 //   * The key sequence is split across CTAs (gridDim.y).  When the splits of an
-//     M-tile form one thread-block cluster (up to kMaxClusterSplits), each CTA
-//     parks its normalised partial O / l (bf16, in 16-column halves of 4 KB)
-//     and its fp32 (m, l) in its own shared memory, then pushes every half
-//     with one bulk copy to the cluster CTA that owns those columns; owners
-//     read all splits' (m, l) through distributed shared memory and finish
-//     their columns of the bf16 output: no partials leave the chip and no
-//     second kernel runs.  Beyond that size each split writes an fp32 partial
-//     to global memory and a merge kernel combines them.  With a single split
-//     the CTA writes the bf16 output directly.
+//     M-tile form one thread-block cluster (up to kMaxClusterSplits), row r of
+//     the tile is finished by cluster CTA r % C: every split stores its
+//     normalised partial O / l of the row (bf16) and its fp32 (m, l) straight
+//     into that CTA's shared memory, which combines the C partials and writes
+//     the bf16 output row.  No partial leaves the chip and no second kernel
+//     runs.  Beyond that size each split writes an fp32 partial to global
+//     memory and a merge kernel combines them.  With a single split the CTA
+//     writes the bf16 output directly.
 //
 // Warp roles (224 threads): warp 0 = copy producer, warp 1 = TMEM allocator and
 // Q K^T issuer, warp 6 = P V issuer, warps 2..5 = softmax and epilogue (TMEM
@@ -56,7 +55,6 @@ namespace {
 
 constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kTilesPerSplit = 3;            // target key tiles per split (on-chip merge)
 constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a cluster
 
 template <int D>
@@ -81,7 +79,7 @@ struct Layout {
 
 // Barrier indices: Q, ring full[NS], ring empty[NS], S full[2], P full[2],
 // PV done[2], drain.
-enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39, B_RECV = 40 };
+enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39 };
 
 // One group of query rows: the action suffix, or a dense batch of language
 // streams.  Its M-tiles occupy workspace rows [row_base, row_base + m_tiles*128).
@@ -116,6 +114,7 @@ struct AttnParams {
   int Hq, G;
   int rows_pad;          // workspace rows of all segments
   int n_splits;
+  int dparts;            // output columns split over dparts CTAs (each computes S in full)
   int fused;             // 1: the splits of an M-tile form a cluster and merge on chip
   float scale_log2;      // log2(e) / sqrt(D)
 };
@@ -165,49 +164,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// Park this thread's row of the split's normalised partial O / l (bf16) and
-// (m, l) in shared memory for the cluster merge.  Layout at `os`: [D/16
-// halves][8 column pairs][128 rows] of bf16x2, so a half is one contiguous
-// 4 KB block (one bulk copy) and a warp's 4-byte stores cover 128 contiguous
-// bytes; (m, l) follow at os + D*256.  With have_o == false the row is zeros
-// (an empty split, l = 0).  Warp-collective (TMEM loads).
-template <int D>
-__device__ __forceinline__ void park_partial(uint32_t os, uint32_t t_row, int row, float m, float l,
-                                             bool have_o) {
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-  for (int c = 0; c < D; c += 32) {
-    float o[32];
-    if (have_o) {
-      tmem_ld32(t_row + c, o);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = 0.f;
-    }
-#pragma unroll
-    for (int pr = 0; pr < 16; ++pr) {
-      const int col = c + 2 * pr;   // columns col, col+1
-      const uint32_t a = os + (col / 16) * 4096 + ((col % 16) / 2) * 512 + row * 4;
-      asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(pack_bf16x2(o[2 * pr] * inv, o[2 * pr + 1] * inv))
-                   : "memory");
-    }
-  }
-  const uint32_t mla = os + D * 256 + row * 8;
-  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(mla), "f"(m), "f"(l) : "memory");
-  fence_proxy_async_smem();   // the halves leave through the copy engine (async proxy)
-}
-
-// Push `bytes` of this CTA's shared memory to shared memory of a cluster
-// peer (addresses from dsmem_map), completion counted on the peer's mbarrier.
-__device__ __forceinline__ void bulk_push(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                          uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
 // All lanes wait on the barrier, then agree: the warp proceeds only if every
 // lane saw the phase complete.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -236,7 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const SegParams& sg = p.seg[si];
   const int mt = blockIdx.x - (si ? p.seg[0].m_tiles : 0);   // M-tile within the segment
   const int split = blockIdx.y;
-  const int g = blockIdx.z;
+  const int g = blockIdx.z / p.dparts;                 // K/V head
+  const int DV = D / p.dparts;                         // output columns of this CTA
+  const int dcol = (blockIdx.z % p.dparts) * DV;       // first output column
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q), 1);
@@ -250,7 +208,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(BAR(B_PV + i), 1);
     }
     mbar_init(BAR(B_DRAIN), 2);   // one commit from each MMA issuer
-    mbar_init(BAR(B_RECV), 1);    // cluster merge: partial halves pushed to this CTA
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -301,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t tS = tmem + static_cast<uint32_t>(D);    // two buffers of 64 columns
 
   const int qtok = kBM / p.G;   // query tokens per tile
+  // The softmax thread's final row state, for the cluster merge.
+  float fin_m = -INFINITY, fin_l = 0.f;
+  bool fin_have = false;
 
   if (n > 0 && warp == 0) {
     // ------------------------------------------------------------ producer
@@ -321,16 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             break;
           }
           const uint32_t dst = sRing + slot * Lay::TILE;
-          mbar_arrive_expect_tx(BAR(B_FULL + slot), Lay::TILE);
+          // K: all D/64 column blocks; V: only the blocks of this CTA's columns.
+          const int kb0 = kv ? dcol / 64 : 0;
+          const int nkb = kv ? DV / 64 : Lay::KB;
+          mbar_arrive_expect_tx(BAR(B_FULL + slot), static_cast<uint32_t>(nkb * 8192));
           const uint8_t* tiles = ti.region < 2 ? (kv ? p.v_tiles[ti.region] : p.k_tiles[ti.region]) : nullptr;
           if (tiles) {
-            bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE,
-                      Lay::TILE, BAR(B_FULL + slot));
+            bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE +
+                               kb0 * 8192,
+                      static_cast<uint32_t>(nkb * 8192), BAR(B_FULL + slot));
           } else {
             const CUtensorMap* tm = ti.region == 2 ? (kv ? &sg.tm_vp : &sg.tm_kp)
                                                    : (kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region]);
-            for (int kb = 0; kb < Lay::KB; ++kb)
-              tma_load_4d(dst + kb * 8192, tm, kb * 64, g, ti.phys0, lay, BAR(B_FULL + slot));
+            for (int kb = 0; kb < nkb; ++kb)
+              tma_load_4d(dst + kb * 8192, tm, (kb0 + kb) * 64, g, ti.phys0, lay, BAR(B_FULL + slot));
           }
           issued = it + 1;
         }
@@ -377,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   } else if (n > 0 && warp == 6) {
     // ------------------------------------------------------------ P V issuer
     if (lane == 0) {
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, false, true);
+      const uint32_t kIdescO = idesc_bf16_f32(kBM, DV, false, true);
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         if (!mbar_wait(BAR(B_PF + st), (j >> 1) & 1, abort_flag)) break;
@@ -468,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (!warp_wait(BAR(B_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < DV; c += 32) {
           float o[32];
           tmem_ld32(tO + c + lane_off, o);
 #pragma unroll
@@ -505,10 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       if (p.n_splits == 1) {
         const int tok = Rs / p.G;
         const int h = g * p.G + Rs % p.G;
-        __nv_bfloat16* dst = sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D;
+        __nv_bfloat16* dst = sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D + dcol;
         const float inv = l > 0.f ? 1.f / l : 0.f;   // a row with no key at all gets zeros
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < DV; c += 32) {
           float o[32];
           tmem_ld32(tO + c + lane_off, o);
           if (row_valid) {
@@ -522,13 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           }
         }
       } else if (p.fused) {
-        park_partial<D>(base + Lay::OFF_Q, tO + lane_off, row, m_used, l, true);
+        fin_m = m_used;   // O stays in TMEM until the merge
+        fin_l = l;
+        fin_have = true;
       } else {
         // Partial O is stored column-major per split ([D][rows_pad]): for each
         // column the 32 lanes of a warp write 32 consecutive rows (128 B).
-        float* dst = p.part_o + (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad * D + R;
+        float* dst = p.part_o + (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad * D +
+                     static_cast<size_t>(dcol) * p.rows_pad + R;
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < DV; c += 32) {
           float o[32];
           tmem_ld32(tO + c + lane_off, o);
           if (row_valid) {
@@ -536,108 +503,128 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(c + i) * p.rows_pad] = o[i];
           }
         }
-        if (row_valid) p.part_ml[part_idx] = make_float2(m_used, l);
+        if (row_valid && dcol == 0) p.part_ml[part_idx] = make_float2(m_used, l);
       }
-    } else if (p.fused) {
-      // empty (or abandoned) split: zeros with l = 0 contribute nothing
-      park_partial<D>(base + Lay::OFF_Q, tO + lane_off, row, -INFINITY, 0.f, false);
-    } else if (n == 0 && row_valid && p.n_splits > 1) {
+    } else if (n == 0 && row_valid && p.n_splits > 1 && dcol == 0) {
       p.part_ml[part_idx] = make_float2(-INFINITY, 0.f);   // empty split: merge skips it
     }
   }
 
   if (p.fused) {
     // ---------------------------------------------------------- cluster merge
-    // Each CTA owns the 16-column halves rank, rank + C, ... of the output.
-    // After barrier 1 every CTA pushes each of its parked halves (4 KB) into
-    // the owner's receive slot [local half][source rank]; the owner combines
-    // them from its own shared memory.  All threads of all CTAs of the
-    // cluster pass both barriers, whatever path they took above.
+    // Row r of the M-tile is finished by cluster CTA r % C.  Once every CTA of
+    // the cluster is past its key loop (barrier 1: their rings are free),
+    // each softmax thread stores its row's normalised partial O / l as bf16
+    // and its (m, l) straight into the owner's shared memory; after barrier 2
+    // each owner combines the C partials of its rows from its own shared
+    // memory and writes whole output rows.  Owner layout: rows [C][rows_max]
+    // of D bf16 with the 16-byte pieces of local row i permuted by
+    // piece ^ (i & 7) (conflict-free stores and loads), then (m, l) [C][rows_max],
+    // then the weights [rows_max][16].  All threads of all CTAs of the cluster
+    // pass both barriers, whatever path they took above.
+    const int kPieces = DV / 8;      // 16-byte pieces of a row
     const int C = p.n_splits;
-    const uint32_t rank = cluster_ctarank();
-    const int owned = (D / 16 - static_cast<int>(rank) + C - 1) / C;
-    const uint32_t os_local = base + Lay::OFF_Q;
-    const uint32_t recv_local = os_local + D * 256 + 1024;
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(BAR(B_RECV), owned * C * 4096);
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int rows_max = (kBM + C - 1) / C;
+    const uint32_t recv = sRing;
+    const uint32_t mlb = recv + static_cast<uint32_t>(C * rows_max * DV * 2);
+    const uint32_t wtb = mlb + static_cast<uint32_t>(C * rows_max * 8);   // weights [rows_max][16]
     __syncwarp();
-    cluster_sync_all();
-    if (threadIdx.x == 0) {
-      for (int half = 0; half < D / 16; ++half) {
-        const uint32_t owner = static_cast<uint32_t>(half % C);
-        const uint32_t slot = static_cast<uint32_t>((half / C) * C) + rank;
-        bulk_push(dsmem_map(recv_local + slot * 4096, owner), os_local + half * 4096, 4096,
-                  dsmem_map(BAR(B_RECV), owner));
-      }
-    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
     if (warp >= 2 && warp <= 5) {
       const int quarter = warp & 3;
       const int row = quarter * 32 + lane;
-      const int Rs = mt * kBM + row;
-      const uint32_t ml_local = os_local + D * 256 + row * 8;
-      float ms[kMaxClusterSplits], ws[kMaxClusterSplits];
-      float M = -INFINITY;
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+      const bool valid = mt * kBM + row < sg.rows;   // padding rows send nothing
+      const uint32_t owner = static_cast<uint32_t>(row % C);
+      const int i = row / C;
+      const uint32_t dst = dsmem_map(recv + static_cast<uint32_t>((rank * rows_max + i) * DV * 2), owner);
+      const float inv = fin_l > 0.f ? 1.f / fin_l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < DV; c += 32) {
+        float o[32];
+        if (fin_have) {   // warp-uniform: the TMEM load is warp-collective
+          tmem_ld32(tO + c + lane_off, o);
+        } else {
 #pragma unroll
-      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-        ws[s2] = 0.f;
-        ms[s2] = -INFINITY;
-        if (s2 < C) {
-          const float2 v = dsmem_ld_f32x2(dsmem_map(ml_local, s2));
-          if (v.y > 0.f) {
-            ms[s2] = v.x;
-            ws[s2] = v.y;
-            M = fmaxf(M, v.x);
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int k = c / 8 + q;
+            dsmem_st_v4(dst + static_cast<uint32_t>(((k ^ (i & 7)) << 4)),
+                        pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                        pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                        pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                        pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
           }
         }
       }
-      // Weight of split s: 2^(m_s - M) l_s / L (the parked partials are O_s / l_s).
-      float L = 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-        const float w = ws[s2] > 0.f ? exp2f(ms[s2] - M) * ws[s2] : 0.f;
-        L += w;
-        ws[s2] = w;
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
-#pragma unroll
-      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) ws[s2] *= inv;
-      const bool row_valid = Rs < sg.rows;
-      const int tok = Rs / p.G, h = g * p.G + Rs % p.G;
-      const bool got = warp_wait(BAR(B_RECV), 0, abort_flag);
-      for (int k = 0; got && k < owned; ++k) {
-        const int half = static_cast<int>(rank) + k * C;
-        float acc[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-          if (s2 < C) {
-            const uint32_t src = recv_local + (k * C + s2) * 4096 + row * 4;
-#pragma unroll
-            for (int pr = 0; pr < 8; ++pr) {
-              uint32_t v;
-              asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src + pr * 512) : "memory");
-              acc[2 * pr] = fmaf(ws[s2], __uint_as_float(v << 16), acc[2 * pr]);
-              acc[2 * pr + 1] = fmaf(ws[s2], __uint_as_float(v & 0xFFFF0000u), acc[2 * pr + 1]);
-            }
-          }
-        }
-        if (row_valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D + half * 16);
-          d4[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-          d4[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                             pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
-        }
-      }
-    }
-    // Every push into this CTA must land before it leaves barrier 2 (an
-    // abandoned wait above still drains here, bounded).
-    if (threadIdx.x == 0) {
-      volatile int no_abort = 0;
-      mbar_wait(BAR(B_RECV), 0, &no_abort);
+      if (valid)
+        dsmem_st_f32x2(dsmem_map(mlb + static_cast<uint32_t>((rank * rows_max + i) * 8), owner),
+                       fin_have ? fin_m : -INFINITY, fin_have ? fin_l : 0.f);
     }
     __syncwarp();
-    cluster_sync_all();   // peers may still read this CTA's shared memory until here
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (warp >= 2 && warp <= 5) {
+      const int t = threadIdx.x - 64;                       // 0..127
+      const int rows_own = (kBM - rank + C - 1) / C;        // rows r with r % C == rank
+      // Weight of split s for local row i: 2^(m_s - M) l_s / sum (the
+      // partials are O_s / l_s).  One half-warp per row, lane s holding split
+      // s (splits >= C weigh 0): max and sum by shuffles.
+      const float2* ml_s = reinterpret_cast<const float2*>(gbase + (mlb - base));
+      float* wt_s = reinterpret_cast<float*>(gbase + (wtb - base));   // [rows_max][16]
+      const uint8_t* recv_s = gbase + (recv - base);
+      for (int pb = t & ~31; pb < rows_own * kMaxClusterSplits; pb += 128) {   // warp-uniform bound
+        const int pair = pb + lane;
+        const bool in = pair < rows_own * kMaxClusterSplits;
+        const int i = in ? pair / kMaxClusterSplits : 0, s2 = pair % kMaxClusterSplits;
+        const float2 v = ml_s[min(s2, C - 1) * rows_max + i];   // in bounds; invalid rows are never read back
+        const bool live = in && s2 < C && v.y > 0.f;
+        float M = live ? v.x : -INFINITY;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, 16));
+        const float e = live ? exp2f(v.x - M) * v.y : 0.f;
+        float L = e;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o, 16);
+        if (in) wt_s[pair] = L > 0.f ? e / L : 0.f;   // a row with no key at all gets zeros
+      }
+      named_bar_sync(1, 128);
+      for (int item = t; item < rows_own * kPieces; item += 128) {
+        const int i = item / kPieces, k = item % kPieces;
+        const int Rs = mt * kBM + i * C + rank;
+        if (Rs >= sg.rows) continue;
+        // All loads first (splits >= C read split C-1 in bounds and weigh 0).
+        const uint8_t* src = recv_s + i * DV * 2 + ((k ^ (i & 7)) << 4);
+        uint4 pv[kMaxClusterSplits];
+        float w[kMaxClusterSplits];
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+          pv[s2] = *reinterpret_cast<const uint4*>(src + min(s2, C - 1) * rows_max * DV * 2);
+          w[s2] = wt_s[i * kMaxClusterSplits + s2];
+        }
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+          const uint32_t vv[4] = {pv[s2].x, pv[s2].y, pv[s2].z, pv[s2].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = fmaf(w[s2], __uint_as_float(vv[e] << 16), acc[2 * e]);
+            acc[2 * e + 1] = fmaf(w[s2], __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
+          }
+        }
+        const int tok = Rs / p.G, h = g * p.G + Rs % p.G;
+        *reinterpret_cast<uint4*>(sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D + dcol + k * 8) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+      }
+    }
   }
 
   tc_fence_before();
@@ -733,7 +720,7 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
       attr_err = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  dim3 grid(m_tiles, prm.n_splits, Hkv);
+  dim3 grid(m_tiles, prm.n_splits, Hkv * prm.dparts);
   cudaError_t e;
   if (prm.fused) {
     cudaLaunchConfig_t cfg = {};
@@ -765,18 +752,21 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Largest cluster of attention CTAs (one per SM) the device can co-schedule,
-// capped at kMaxClusterSplits; 1 if clusters are unavailable.
+// How many clusters of c attention CTAs (one per SM) the device can hold at
+// once, for c = 1..kMaxClusterSplits (index c); 0 where clusters of that size
+// cannot be scheduled.  Clusters live within one GPC, so this is not simply
+// SMs / c.  Queried once per head dimension.
 template <int D>
-int max_cluster_splits() {
-  static int cached = -1;
+const int* cluster_capacity() {
+  static int cap[kMaxClusterSplits + 1];
+  static bool done = false;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached >= 0) return cached;
-  cached = 1;
+  if (done) return cap;
   cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::ALLOC);
   cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  for (int c = kMaxClusterSplits; c >= 2; c /= 2) {
+  cap[0] = 0;
+  for (int c = 1; c <= kMaxClusterSplits; ++c) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, c, 1);
     cfg.blockDim = dim3(kThreads);
@@ -789,13 +779,23 @@ int max_cluster_splits() {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<D>, &cfg) == cudaSuccess && n >= 1) {
-      cached = c;
-      break;
-    }
+    cap[c] = cudaOccupancyMaxActiveClusters(&n, attn_kernel<D>, &cfg) == cudaSuccess ? n : 0;
   }
   cudaGetLastError();
-  return cached;
+  done = true;
+  return cap;
+}
+
+// Relative cost of one launch in units of "one K tile plus one full V tile
+// streamed into an SM": tiles * (1 + 1/dparts) for the key loop, and with a
+// cluster merge the partial exchange (the full-width partial costs about
+// 9.5 units) plus the merge's fixed barriers and combine (about 6 units).
+// Fitted to timings of the 2163-key suffix on GB300.
+double split_cost(int t_max, int splits, int dparts) {
+  const int tiles = (t_max + splits - 1) / splits;
+  double c = tiles * (1.0 + 1.0 / dparts);
+  if (splits > 1) c += 9.5 / dparts + 6.0;
+  return c;
 }
 
 }  // namespace
@@ -869,27 +869,52 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   prm.G = G;
   prm.rows_pad = m_total * kBM;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
-  // Split the key sequence: about kTilesPerSplit 64-key tiles per CTA (the
-  // per-CTA set-up, Q load and partial write amortise over them), at most one
-  // wave of CTAs.
-  const int wave = a.num_sms / (m_total * a.Hkv);
-  int splits = a.forced_splits > 0 ? a.forced_splits : (t_max + kTilesPerSplit - 1) / kTilesPerSplit;
-  if (a.forced_splits <= 0 && splits > wave) splits = wave;
-  splits = splits < 1 ? 1 : splits;
-  splits = splits > t_max ? t_max : splits;
-  int cmax = 1;
+  // Partition: `splits` slices of the key sequence (a cluster that merges on
+  // chip) times `dparts` shares of the output columns per (tile, head).  The
+  // automatic choice minimises split_cost over the partitions whose clusters
+  // all fit on the device at once (one wave).
+  const int* cap = nullptr;
   switch (a.D) {
-    case 64: cmax = max_cluster_splits<64>(); break;
-    case 128: cmax = max_cluster_splits<128>(); break;
-    case 256: cmax = max_cluster_splits<256>(); break;
+    case 64: cap = cluster_capacity<64>(); break;
+    case 128: cap = cluster_capacity<128>(); break;
+    case 256: cap = cluster_capacity<256>(); break;
     default: return cudaErrorInvalidValue;
   }
-  // Prefer an on-chip (cluster) merge: cap the automatic split count there.
-  if (a.forced_splits <= 0 && splits > cmax && cmax >= 2) splits = cmax;
-  const bool fused = splits >= 2 && splits <= cmax;
-  if (!fused) splits = splits > a.max_splits ? a.max_splits : splits;
+  const int units = m_total * a.Hkv;
+  auto fits = [&](int sp, int dp) {
+    if (sp == 1) return units * dp <= a.num_sms;
+    return sp <= kMaxClusterSplits && units * dp <= cap[sp];
+  };
+  int splits = a.forced_splits > 0 ? a.forced_splits : 0;
+  int dparts = a.forced_dparts > 0 ? a.forced_dparts : 0;
+  if (splits == 0 || dparts == 0) {
+    double best = 1e30;
+    int bs = 1, bd = 1;
+    const int s_hi = t_max < kMaxClusterSplits ? t_max : kMaxClusterSplits;
+    for (int sp = 1; sp <= s_hi; ++sp) {
+      if (splits > 0 && sp != splits) continue;
+      for (int dp = 1; dp <= 4; dp *= 2) {
+        if (dparts > 0 && dp != dparts) continue;
+        if (a.D / dp < 64 || !fits(sp, dp)) continue;
+        const double c = split_cost(t_max, sp, dp);
+        if (c < best - 1e-9) {
+          best = c;
+          bs = sp;
+          bd = dp;
+        }
+      }
+    }
+    if (splits == 0) splits = bs;
+    if (dparts == 0) dparts = bd;
+  }
+  splits = splits > t_max ? t_max : splits;
   splits = splits < 1 ? 1 : splits;
+  const bool fused = splits >= 2 && splits <= kMaxClusterSplits && cap[splits] >= 1;
+  if (!fused) splits = splits > a.max_splits ? a.max_splits : splits;
+  if (dparts != 1 && dparts != 2 && dparts != 4) return cudaErrorInvalidValue;
+  if (a.D % (dparts * 64) != 0) return cudaErrorInvalidValue;
   prm.n_splits = splits;
+  prm.dparts = dparts;
   prm.fused = fused ? 1 : 0;
   if (used_splits) *used_splits = splits;
   switch (a.D) {

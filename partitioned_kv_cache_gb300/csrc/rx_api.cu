@@ -130,6 +130,7 @@ struct rx_cache {
   int P = 0;             // pinned tokens currently held
   long long host_pushes = 0;
   int forced_splits = 0;
+  int forced_dparts = 0;
 };
 
 #define RX_GUARD_BEGIN try {
@@ -373,6 +374,7 @@ static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   a.part_ml = h->part_ml;
   a.max_splits = h->max_splits;
   a.forced_splits = h->forced_splits;
+  a.forced_dparts = h->forced_dparts;
   a.num_sms = h->num_sms;
   return a;
 }
@@ -674,6 +676,17 @@ rx_status rx_set_attn_splits(rx_cache_t h, int splits) {
   if (splits < 0 || splits > h->max_splits)
     return fail(RX_ERR_ARG, "rx_set_attn_splits: %d not in [0, %d]", splits, h->max_splits);
   h->forced_splits = splits;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_set_attn_dparts(rx_cache_t h, int dparts) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_set_attn_dparts: null cache");
+  if (!(dparts == 0 || dparts == 1 || dparts == 2 || dparts == 4) || (dparts > 0 && h->cfg.D / dparts < 64))
+    return fail(RX_ERR_ARG, "rx_set_attn_dparts: %d not 0, or 1/2/4 with D/dparts >= 64 (D = %d)", dparts,
+                h->cfg.D);
+  h->forced_dparts = dparts;
   return RX_OK;
   RX_GUARD_END
 }

@@ -134,6 +134,7 @@ struct AttnLaunch {
   float2* part_ml;    // workspace: [Hkv][splits][tiles*128]
   int max_splits;     // capacity of the workspace in splits
   int forced_splits;  // 0 = automatic
+  int forced_dparts;  // output-column split: 0 = automatic, else 1, 2 or 4
   int num_sms;
 };
 

@@ -30,7 +30,8 @@ EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_fram
            "rx_get_state", "rx_debug_window", "rx_export_window", "rx_check_device_error",
            "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
            "rx_attend_regions_static", "rx_attend_suffix_block_causal", "rx_tail_append",
-           "rx_snapshot_bytes", "rx_snapshot", "rx_restore", "rx_push_frame_async")
+           "rx_snapshot_bytes", "rx_snapshot", "rx_restore", "rx_push_frame_async",
+           "rx_set_attn_dparts")
 
 
 class RxConfig(ctypes.Structure):
@@ -61,6 +62,7 @@ _sigs = {
     "rx_export_window": (_i, [_vp, _i, _vp, _vp, _vp]),
     "rx_check_device_error": (_i, [_vp, ctypes.POINTER(_i), _vp]),
     "rx_set_attn_splits": (_i, [_vp, _i]),
+    "rx_set_attn_dparts": (_i, [_vp, _i]),
     "rx_launch_count": (ctypes.c_longlong, []),
     "rx_status_str": (ctypes.c_char_p, [_i]),
     "rx_last_error": (ctypes.c_char_p, []),
@@ -257,6 +259,9 @@ class Cache:
 
     def set_attn_splits(self, splits: int) -> None:
         _check(_lib.rx_set_attn_splits(self._h, splits), "rx_set_attn_splits")
+
+    def set_attn_dparts(self, dparts: int) -> None:
+        _check(_lib.rx_set_attn_dparts(self._h, dparts), "rx_set_attn_dparts")
 
 
 def ada_gamma(t: torch.Tensor, state: torch.Tensor, W1: torch.Tensor, b1: torch.Tensor,

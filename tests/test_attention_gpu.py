@@ -93,6 +93,40 @@ def test_split_count_does_not_change_the_result(rx, splits):
     cache.close()
 
 
+@pytest.mark.parametrize("splits,dparts", [(12, 1), (12, 2), (12, 4), (1, 2), (1, 4), (3, 4),
+                                           (20, 2), (20, 4), (0, 0)])
+def test_output_column_split_does_not_change_the_result(rx, splits, dparts):
+    """Every CTA of a (tile, split) computes the scores in full and the value
+    product for its D/dparts columns: fused cluster merge (12, 3 splits),
+    single split (1) and the global-memory merge (20 splits) all agree with
+    the oracle."""
+    wl = W.WORKLOADS["c2"]
+    seed = 9
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(splits)
+    cache.set_attn_dparts(dparts)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    got = host64(_attend(cache, wl, seed, wl.N, 1, 0))
+    check_attention(got, _oracle_attend(ost, wl, seed, wl.N, 1, 0))
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
+def test_dparts_argument_errors(rx):
+    wl = W.WORKLOADS["c1"]   # D = 64: only one 64-column part
+    cache = _make(rx, wl, 10)
+    for bad in (-1, 3, 2, 4, 8):
+        with pytest.raises(rx.RxError):
+            cache.set_attn_dparts(bad)
+    cache.set_attn_dparts(1)
+    cache.set_attn_dparts(0)
+    cache.close()
+
+
 @pytest.mark.parametrize("S", [1, 7, 16, 17, 50, 51])
 def test_ragged_suffix_lengths(rx, S):
     wl = W.WORKLOADS["c2"]
