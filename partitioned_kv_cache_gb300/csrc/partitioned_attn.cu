@@ -24,14 +24,16 @@
 //     running maximum grows by more than 2^8 (otherwise the stale maximum is
 //     kept: exact after the final division by the row sum).
 //   * The key sequence is split across CTAs (gridDim.y).  When the splits of an
-//     M-tile form one thread-block cluster (up to kMaxClusterSplits), row r of
-//     the tile is finished by cluster CTA r % C: every split stores its
-//     normalised partial O / l of the row (bf16) and its fp32 (m, l) straight
-//     into that CTA's shared memory, which combines the C partials and writes
-//     the bf16 output row.  No partial leaves the chip and no second kernel
-//     runs.  Beyond that size each split writes an fp32 partial to global
-//     memory and a merge kernel combines them.  With a single split the CTA
-//     writes the bf16 output directly.
+//     M-tile form one thread-block cluster (up to kMaxClusterSplits), every
+//     split writes its normalised partial O / l (bf16) and fp32 (m, l) to an
+//     exchange area in L2, the cluster passes one barrier, and each CTA then
+//     combines a block of rows from all C partials and writes the bf16
+//     output: no second kernel runs.  Beyond that size each split writes an
+//     fp32 partial to global memory and a merge kernel combines them.  With a
+//     single split the CTA writes the bf16 output directly.
+//   * The output columns of a (tile, split) may be shared by dparts CTAs: each
+//     computes S in full but loads only its D/dparts columns of V, so its key
+//     loop moves fewer bytes and its partial is dparts times smaller.
 //
 // Warp roles (224 threads): warp 0 = copy producer, warp 1 = TMEM allocator and
 // Q K^T issuer, warp 6 = P V issuer, warps 2..5 = softmax and epilogue (TMEM
@@ -512,35 +514,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (p.fused) {
     // ---------------------------------------------------------- cluster merge
-    // Row r of the M-tile is finished by cluster CTA r % C.  Once every CTA of
-    // the cluster is past its key loop (barrier 1: their rings are free),
-    // each softmax thread stores its row's normalised partial O / l as bf16
-    // and its (m, l) straight into the owner's shared memory; after barrier 2
-    // each owner combines the C partials of its rows from its own shared
-    // memory and writes whole output rows.  Owner layout: rows [C][rows_max]
-    // of D bf16 with the 16-byte pieces of local row i permuted by
-    // piece ^ (i & 7) (conflict-free stores and loads), then (m, l) [C][rows_max],
-    // then the weights [rows_max][16].  All threads of all CTAs of the cluster
-    // pass both barriers, whatever path they took above.
+    // The C splits of this (tile, head, column share) exchange their partials
+    // through L2: each softmax thread writes its row's normalised partial
+    // O / l (bf16) and (m, l) to this split's slot of the exchange area, one
+    // cluster barrier, then cluster CTA o combines rows [o*per, (o+1)*per) of
+    // the C slots and writes the bf16 output.  Exchange layout per cluster:
+    // O [C][D/8 / dparts pieces][128 rows] of 16 bytes (a warp's store is 512
+    // contiguous bytes), then (m, l) [C][128].  All threads of all CTAs of
+    // the cluster pass the barrier, whatever path they took above.
     const int kPieces = DV / 8;      // 16-byte pieces of a row
     const int C = p.n_splits;
     const int rank = static_cast<int>(cluster_ctarank());
-    const int rows_max = (kBM + C - 1) / C;
-    const uint32_t recv = sRing;
-    const uint32_t mlb = recv + static_cast<uint32_t>(C * rows_max * DV * 2);
-    const uint32_t wtb = mlb + static_cast<uint32_t>(C * rows_max * 8);   // weights [rows_max][16]
-    __syncwarp();
-    cluster_arrive_release();
-    cluster_wait_acquire();
+    const size_t cid = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
+    uint4* xo = reinterpret_cast<uint4*>(p.part_o) + cid * C * kPieces * kBM;
+    float2* xml = reinterpret_cast<float2*>(reinterpret_cast<uint4*>(p.part_o) +
+                                            static_cast<size_t>(gridDim.x) * gridDim.z * C * kPieces * kBM) +
+                  cid * C * kBM;
     if (warp >= 2 && warp <= 5) {
       const int quarter = warp & 3;
       const int row = quarter * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-      const bool valid = mt * kBM + row < sg.rows;   // padding rows send nothing
-      const uint32_t owner = static_cast<uint32_t>(row % C);
-      const int i = row / C;
-      const uint32_t dst = dsmem_map(recv + static_cast<uint32_t>((rank * rows_max + i) * DV * 2), owner);
+      const bool valid = mt * kBM + row < sg.rows;   // padding rows are never read
       const float inv = fin_l > 0.f ? 1.f / fin_l : 0.f;
+      uint4* dst = xo + static_cast<size_t>(rank) * kPieces * kBM + row;
 #pragma unroll 1
       for (int c = 0; c < DV; c += 32) {
         float o[32];
@@ -552,71 +548,63 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int k = c / 8 + q;
-            dsmem_st_v4(dst + static_cast<uint32_t>(((k ^ (i & 7)) << 4)),
-                        pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
-                        pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                        pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                        pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
-          }
+          for (int q = 0; q < 4; ++q)
+            dst[static_cast<size_t>(c / 8 + q) * kBM] =
+                make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                           pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                           pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                           pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
         }
       }
-      if (valid)
-        dsmem_st_f32x2(dsmem_map(mlb + static_cast<uint32_t>((rank * rows_max + i) * 8), owner),
-                       fin_have ? fin_m : -INFINITY, fin_have ? fin_l : 0.f);
+      if (valid) xml[rank * kBM + row] = make_float2(fin_have ? fin_m : -INFINITY, fin_have ? fin_l : 0.f);
     }
     __syncwarp();
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    if (warp >= 2 && warp <= 5) {
-      const int t = threadIdx.x - 64;                       // 0..127
-      const int rows_own = (kBM - rank + C - 1) / C;        // rows r with r % C == rank
-      // Weight of split s for local row i: 2^(m_s - M) l_s / sum (the
-      // partials are O_s / l_s).  One half-warp per row, lane s holding split
-      // s (splits >= C weigh 0): max and sum by shuffles.
-      const float2* ml_s = reinterpret_cast<const float2*>(gbase + (mlb - base));
-      float* wt_s = reinterpret_cast<float*>(gbase + (wtb - base));   // [rows_max][16]
-      const uint8_t* recv_s = gbase + (recv - base);
-      for (int pb = t & ~31; pb < rows_own * kMaxClusterSplits; pb += 128) {   // warp-uniform bound
-        const int pair = pb + lane;
-        const bool in = pair < rows_own * kMaxClusterSplits;
-        const int i = in ? pair / kMaxClusterSplits : 0, s2 = pair % kMaxClusterSplits;
-        const float2 v = ml_s[min(s2, C - 1) * rows_max + i];   // in bounds; invalid rows are never read back
-        const bool live = in && s2 < C && v.y > 0.f;
-        float M = live ? v.x : -INFINITY;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, 16));
-        const float e = live ? exp2f(v.x - M) * v.y : 0.f;
-        float L = e;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o, 16);
-        if (in) wt_s[pair] = L > 0.f ? e / L : 0.f;   // a row with no key at all gets zeros
-      }
-      named_bar_sync(1, 128);
-      for (int item = t; item < rows_own * kPieces; item += 128) {
-        const int i = item / kPieces, k = item % kPieces;
-        const int Rs = mt * kBM + i * C + rank;
+    cluster_sync_all();   // release / acquire: the slots are visible to the whole cluster
+    // Every thread of the CTA finishes at most one (piece k, row i) item per
+    // pass, rows fastest (a warp's loads of one split are consecutive 16-byte
+    // rows).  The C partial pieces and the C (m, l) of the row are loaded
+    // together (splits >= C re-read split C-1 and weigh 0); the weight of
+    // split s is 2^(m_s - M) l_s / sum, as the partials are O_s / l_s.
+    {
+      const int per = (kBM + C - 1) / C;
+      const int r0 = rank * per;
+      const int nr = max(0, min(per, kBM - r0));            // rows this CTA finishes
+      for (int item = threadIdx.x; item < nr * kPieces; item += kThreads) {
+        const int i = item % nr, k = item / nr;
+        const int Rs = mt * kBM + r0 + i;
         if (Rs >= sg.rows) continue;
-        // All loads first (splits >= C read split C-1 in bounds and weigh 0).
-        const uint8_t* src = recv_s + i * DV * 2 + ((k ^ (i & 7)) << 4);
+        const uint4* src = xo + static_cast<size_t>(k) * kBM + r0 + i;
         uint4 pv[kMaxClusterSplits];
-        float w[kMaxClusterSplits];
+        float2 ml[kMaxClusterSplits];
 #pragma unroll
         for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-          pv[s2] = *reinterpret_cast<const uint4*>(src + min(s2, C - 1) * rows_max * DV * 2);
-          w[s2] = wt_s[i * kMaxClusterSplits + s2];
+          const int sc = min(s2, C - 1);
+          pv[s2] = __ldcg(src + static_cast<size_t>(sc) * kPieces * kBM);
+          ml[s2] = __ldcg(xml + sc * kBM + r0 + i);
         }
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+          if (s2 < C && ml[s2].y > 0.f) M = fmaxf(M, ml[s2].x);
+        float w[kMaxClusterSplits];
+        float L = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+          w[s2] = s2 < C && ml[s2].y > 0.f ? exp2f(ml[s2].x - M) * ml[s2].y : 0.f;
+          L += w[s2];
+        }
+        const float invL = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
         for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+          const float ws = w[s2] * invL;
           const uint32_t vv[4] = {pv[s2].x, pv[s2].y, pv[s2].z, pv[s2].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            acc[2 * e] = fmaf(w[s2], __uint_as_float(vv[e] << 16), acc[2 * e]);
-            acc[2 * e + 1] = fmaf(w[s2], __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
+            acc[2 * e] = fmaf(ws, __uint_as_float(vv[e] << 16), acc[2 * e]);
+            acc[2 * e + 1] = fmaf(ws, __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
           }
         }
         const int tok = Rs / p.G, h = g * p.G + Rs % p.G;
@@ -881,9 +869,11 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
     default: return cudaErrorInvalidValue;
   }
   const int units = m_total * a.Hkv;
+  // A cluster merge exchanges its partials through the workspace, which
+  // holds at most max_splits of them.
   auto fits = [&](int sp, int dp) {
     if (sp == 1) return units * dp <= a.num_sms;
-    return sp <= kMaxClusterSplits && units * dp <= cap[sp];
+    return sp <= kMaxClusterSplits && sp <= a.max_splits && units * dp <= cap[sp];
   };
   int splits = a.forced_splits > 0 ? a.forced_splits : 0;
   int dparts = a.forced_dparts > 0 ? a.forced_dparts : 0;
@@ -908,9 +898,9 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
     if (dparts == 0) dparts = bd;
   }
   splits = splits > t_max ? t_max : splits;
+  splits = splits > a.max_splits ? a.max_splits : splits;
   splits = splits < 1 ? 1 : splits;
   const bool fused = splits >= 2 && splits <= kMaxClusterSplits && cap[splits] >= 1;
-  if (!fused) splits = splits > a.max_splits ? a.max_splits : splits;
   if (dparts != 1 && dparts != 2 && dparts != 4) return cudaErrorInvalidValue;
   if (a.D % (dparts * 64) != 0) return cudaErrorInvalidValue;
   prm.n_splits = splits;
