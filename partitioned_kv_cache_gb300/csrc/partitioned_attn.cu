@@ -776,13 +776,13 @@ const int* cluster_capacity() {
 
 // Relative cost of one launch in units of "one K tile plus one full V tile
 // streamed into an SM": tiles * (1 + 1/dparts) for the key loop, and with a
-// cluster merge the partial exchange (the full-width partial costs about
-// 9.5 units) plus the merge's fixed barriers and combine (about 6 units).
-// Fitted to timings of the 2163-key suffix on GB300.
+// cluster merge the exchange of the partials through L2 (about 2.25 units for
+// a full-width partial) plus the merge's barrier and combine (about 2.5
+// units).  Fitted to timings of 2163- and 8448-key suffixes on GB300.
 double split_cost(int t_max, int splits, int dparts) {
   const int tiles = (t_max + splits - 1) / splits;
   double c = tiles * (1.0 + 1.0 / dparts);
-  if (splits > 1) c += 9.5 / dparts + 6.0;
+  if (splits > 1) c += 2.25 / dparts + 2.5;
   return c;
 }
 
