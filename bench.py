@@ -251,6 +251,24 @@ def run_reference(args, wl):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: barrier, then a MAX all-reduce (replicas run
+    the same work, so the job is as fast as its slowest GPU)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    dist.barrier()
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job units per second: every rank processed units_per_rank."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -371,14 +389,8 @@ def run_ours(args, wl):
     e1.synchronize()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        dist.barrier()
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    total_steps = args.steps * K * world
-    value = total_steps / (ms / 1e3)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    value = replica_throughput(args.steps * K, world, ms)
 
     # ---------------- attention alone: per-launch time for the roofline ----------------
     reps = max(3, min(50, args.steps // 10))
@@ -475,8 +487,8 @@ def run_ours(args, wl):
             h_out.copy_(o[s, K - 1, L - 1], non_blocking=True)
         f1.record(stream)
     f1.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    e2e_val = e2e_steps * K * world / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
+    e2e_val = replica_throughput(e2e_steps * K, world, e2e_ms)
     assert cache.check_device_error() == 0, "a kernel reported a device-side timeout"
 
     if rank != 0:
