@@ -238,10 +238,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   grid_launch_dependents();
   // Key tiles of this split.  The window comes from the device-side ring state
   // published by the append kernel (one 64-bit word: a consistent snapshot
-  // even while a push on another stream is publishing).
-  int head = 0, valid = 0;
-  load_ring_state(p.st, &head, &valid);
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");   // frame data before the snapshot
+  // even while a push on another stream is publishing).  Pushes in stream
+  // order completed before the dependency wait above; only a cache with a
+  // spare slot takes pushes concurrently, and there the frame data must be
+  // ordered after the snapshot.
+  // One thread per CTA reads the word (every CTA of the grid reads the same
+  // line) and hands it to the others through shared memory.
+  volatile int* ring_word = reinterpret_cast<volatile int*>(gbase + Lay::OFF_MISC + 8);
+  if (threadIdx.x == 0) {
+    int h = 0, v = 0;
+    load_ring_state(p.st, &h, &v);
+    if (p.slots > p.N) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    ring_word[0] = h;
+    ring_word[1] = v;
+  }
+  __syncthreads();
+  const int head = ring_word[0], valid = ring_word[1];
   // With a spare slot and a full ring the window is every slot but `head`.
   const bool hole = p.slots > p.N && valid == p.N;
   const int win_len = hole ? (p.slots - 1) * p.F : valid * p.F;
