@@ -20,9 +20,16 @@
 // 64 tokens, 128-byte rows, chunk ^ (token & 7) swizzle), so that the
 // attention kernel moves a whole tile with one bulk copy.  The same packing
 // serves the one-time pinned-prefix copy.
+//
+// When whole tiles are written (F, or the start token, a multiple of 64) the
+// tensor-memory-access unit does the re-layout: one CTA per destination tile
+// loads the source tokens as 128-byte-swizzled boxes, which is exactly the
+// tile layout, and stores the tile back with one bulk copy.  Otherwise a
+// thread per 16-byte chunk computes the tiled offset.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "rx_internal.h"
 #include "sm103_ptx.cuh"
@@ -142,11 +149,93 @@ __global__ void __launch_bounds__(kThreads) unpack_tiles_kernel(
   }
 }
 
+// One CTA per destination tile: blockIdx.x = source tile (64 tokens),
+// blockIdx.y = layer * Hkv + head, blockIdx.z = K (0) or V (1).
+struct PackTma {
+  CUtensorMap tm[2];    // sources (D, Hkv, n, L), box (64, 1, 64, 1), 128-byte swizzle
+  uint8_t* dst[2];      // tiled regions
+  DevState* st;         // ring append when non-null
+  int Hkv, D, T, tok0, F, N, slots;
+};
+
+__global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constant__ PackTma a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // swizzle atoms are 1 KB
+  const uint32_t bar = base + static_cast<uint32_t>(tile_bytes(a.D));
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (threadIdx.x != 0) return;
+  int head = 0, valid = 0;
+  if (a.st) load_ring_state(a.st, &head, &valid);
+  const int base_tok = a.st ? head * a.F : a.tok0;   // a multiple of 64 (host-checked)
+  const int l = blockIdx.y / a.Hkv, g = blockIdx.y % a.Hkv, kv = blockIdx.z;
+  const uint32_t bytes = static_cast<uint32_t>(tile_bytes(a.D));
+  mbar_init(bar, 1);
+  fence_barrier_init();
+  mbar_arrive_expect_tx(bar, bytes);
+  for (int kb = 0; kb < a.D / 64; ++kb)
+    tma_load_4d(base + kb * 8192, &a.tm[kv], kb * 64, g, blockIdx.x * kTileTok, l, bar);
+  volatile int gave_up = 0;
+  const bool ok = mbar_wait(bar, 0, &gave_up);
+  if (ok) {
+    uint8_t* dst = a.dst[kv] + ((static_cast<long long>(l) * a.Hkv + g) * a.T + base_tok / kTileTok + blockIdx.x) * bytes;
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(base), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the tile is written
+    asm volatile("fence.proxy.async.global;" ::: "memory");    // ... and ordered before what follows
+  } else {
+    // the copy may still land in shared memory: wait for it (bounded) before exiting
+    volatile int no_abort = 0;
+    mbar_wait(bar, 0, &no_abort);
+    if (a.st) atomicOr(&a.st->err, kErrAppendTimeout);
+  }
+  if (!a.st) return;
+  __threadfence();
+  const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+  const unsigned int prev = atomicAdd(&a.st->append_arrivals, 1u);
+  if (prev == total - 1) {
+    // Every CTA wrote its tile and fenced before arriving: publish.
+    __threadfence();
+    publish_ring_state(a.st, head + 1 == a.slots ? 0 : head + 1, valid < a.N ? valid + 1 : a.N);
+    a.st->pushes += 1;
+    a.st->append_arrivals = 0;
+    __threadfence();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pack_tiles(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
                               int L, int n, int Hkv, int D, int T, int tok0, DevState* st, int F,
                               int N, int slots, int num_sms, cudaStream_t s) {
+  // Whole destination tiles: the TMA path.
+  const bool whole = st ? (F % kTileTok == 0) : (tok0 % kTileTok == 0);
+  if (whole && n > 0) {
+    PackTma a;
+    memset(&a, 0, sizeof(a));
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(L)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Hkv) * D * 2,
+                                 static_cast<uint64_t>(n) * Hkv * D * 2};
+    const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(kTileTok), 1u};
+    if (encode_tmap_4d(&a.tm[0], k_src, dims, strides, box) && encode_tmap_4d(&a.tm[1], v_src, dims, strides, box)) {
+      a.dst[0] = static_cast<uint8_t*>(k_dst);
+      a.dst[1] = static_cast<uint8_t*>(v_dst);
+      a.st = st;
+      a.Hkv = Hkv;
+      a.D = D;
+      a.T = T;
+      a.tok0 = tok0;
+      a.F = F;
+      a.N = N;
+      a.slots = slots;
+      const size_t smem = static_cast<size_t>(tile_bytes(D)) + 1024 + 16;
+      const dim3 grid(static_cast<unsigned int>((n + kTileTok - 1) / kTileTok), static_cast<unsigned int>(L * Hkv), 2);
+      const cudaError_t e = launch_k(pack_tiles_tma_kernel, grid, dim3(32), smem, s, a);
+      return e != cudaSuccess ? e : cudaGetLastError();
+    }
+  }
   const long long total = static_cast<long long>(L) * n * Hkv * (D >> 3);
   long long blocks = (total + static_cast<long long>(kThreads) * kVecPerThread - 1) /
                      (static_cast<long long>(kThreads) * kVecPerThread);

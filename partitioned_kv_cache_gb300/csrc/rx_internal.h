@@ -36,6 +36,7 @@ __device__ __forceinline__ void publish_ring_state(DevState* st, int head, int v
 
 constexpr int kErrAttnTimeout = 1;    // attention kernel: a bounded wait gave up
 constexpr int kErrBatchTimeout = 2;   // batched attention: a bounded wait gave up
+constexpr int kErrAppendTimeout = 4;  // ring append: a bounded wait gave up
 
 constexpr int kMaxCond = 16;          // rx_ada_gamma: conditioning vectors per call
 constexpr int kMaxHidden = 2048;      // rx_ada_gamma: hidden width
