@@ -20,9 +20,11 @@
 //     a K slot is released once Q K^T has read it, a V slot once P V has.
 //   * S = Q K^T and O += P V run on tcgen05 with both accumulators in TMEM
 //     (O: D columns; S: two 64-column buffers).  One thread per row does the
-//     online softmax in the exp2 domain; O is rescaled in TMEM only when the
-//     running maximum grows by more than 2^8 (otherwise the stale maximum is
-//     kept: exact after the final division by the row sum).
+//     online softmax in the exp2 domain and writes P (bf16) back to TMEM (two
+//     32-column buffers), where P V reads its A operand: P never touches
+//     shared memory.  O is rescaled in TMEM only when the running maximum
+//     grows by more than 2^8 (otherwise the stale maximum is kept: exact after
+//     the final division by the row sum).
 //   * The key sequence is split across CTAs (gridDim.y).  When the splits of an
 //     M-tile form one thread-block cluster (up to kMaxClusterSplits), every
 //     split writes its normalised partial O / l (bf16) and fp32 (m, l) to an
@@ -58,23 +60,29 @@ namespace {
 constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a cluster
+// Shared memory for the K/V ring.  Two builds of the kernel: 128 KB for key
+// loops of at most kShallowTiles tiles per CTA, which have nothing to gain
+// from a deeper ring and run faster with the smaller allocation, and 160 KB
+// for longer loops, which prefetch one tile deeper.
+constexpr int kRingShallowKB = 128;
+constexpr int kRingDeepKB = 160;
+constexpr int kShallowTiles = 4;
 
-template <int D>
+template <int D, int RING_KB>
 struct Layout {
   static constexpr int KB = D / 64;                 // 64-column blocks of the head dim
   static constexpr int Q_BLOCK = kBM * 128;         // one 64-column block of Q: 128 rows x 128 B
   static constexpr int Q_BYTES = KB * Q_BLOCK;
-  static constexpr int P_BYTES = kBM * kBN * 2;
   static constexpr int TILE = static_cast<int>(tile_bytes(D));   // one K or V tile: [KB][64][128 B]
-  static constexpr int NS = (128 * 1024) / TILE;    // ring slots (4 at D = 256)
+  static constexpr int NS_FIT = (RING_KB * 1024) / TILE;
+  static constexpr int NS = NS_FIT > 16 ? 16 : NS_FIT;   // ring slots (5 at D = 256)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + Q_BYTES;
-  static constexpr int OFF_P = OFF_RING + NS * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NS * TILE;
   static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;        // slack for 1024-byte alignment
-  static constexpr int TMEM_COLS = (D + 2 * kBN) <= 256 ? 256 : 512;
+  static constexpr int TMEM_COLS = (D + 3 * kBN) <= 256 ? 256 : 512;   // O, S x 2, P x 2
   static_assert(ALLOC <= 232448, "shared memory budget");
   static_assert(NS >= 4 && NS <= 16, "ring depth");
 };
@@ -153,6 +161,17 @@ __device__ __forceinline__ TileInfo tile_at(int t, int nt_pin, int nt_win, int P
   return ti;
 }
 
+// O += P V with P (the A operand) read from tensor memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -173,16 +192,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
+template <int D, int RING_KB>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
-  using Lay = Layout<D>;
+  using Lay = Layout<D, RING_KB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + Lay::OFF_Q;
   const uint32_t sRing = base + Lay::OFF_RING;
-  const uint32_t sP = base + Lay::OFF_P;
   const uint32_t sBar = base + Lay::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lay::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lay::OFF_MISC + 4);
@@ -270,17 +288,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem;                               // columns [0, D)
   const uint32_t tS = tmem + static_cast<uint32_t>(D);    // two buffers of 64 columns
+  const uint32_t tP = tS + 2 * kBN;                       // two P buffers of 32 columns (bf16 pairs)
 
   const int qtok = kBM / p.G;   // query tokens per tile
+  const int ns = Lay::NS;   // ring slots
   // The softmax thread's final row state, for the cluster merge.
   float fin_m = -INFINITY, fin_l = 0.f;
   bool fin_have = false;
 
   if (n > 0 && warp == 0) {
     // ------------------------------------------------------------ producer
-    // Ring order: K_0, V_0, K_1, V_1, ...; item i uses slot i % NS.
+    // Ring order: K_0, V_0, K_1, V_1, ...; item i uses slot i % ns.
     if (lane == 0) {
       int issued = 0;
+      int slot = 0, rnd = 0;   // issued % ns and issued / ns, kept without dividing
       mbar_arrive_expect_tx(BAR(B_Q), Lay::Q_BYTES);
       for (int kb = 0; kb < Lay::KB; ++kb)
         tma_load_4d(sQ + kb * Lay::Q_BLOCK, &sg.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
@@ -289,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const int lay = ti.region == 2 ? 0 : p.layer;
         for (int kv = 0; kv < 2; ++kv) {
           const int it = issued;
-          const int slot = it % Lay::NS;
-          if (it >= Lay::NS && !mbar_wait(BAR(B_EMPTY + slot), ((it / Lay::NS) - 1) & 1, abort_flag)) {
+          if (rnd > 0 && !mbar_wait(BAR(B_EMPTY + slot), (rnd - 1) & 1, abort_flag)) {
             issued = -issued - 1;   // stop; remember how many were issued
             break;
           }
@@ -311,28 +331,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
               tma_load_4d(dst + kb * 8192, tm, (kb0 + kb) * 64, g, ti.phys0, lay, BAR(B_FULL + slot));
           }
           issued = it + 1;
+          if (++slot == ns) {
+            slot = 0;
+            ++rnd;
+          }
         }
       }
       if (issued < 0) issued = -issued - 1;
       // Every copy issued must land before the CTA exits, even after an abort.
       volatile int no_abort = 0;
       mbar_wait(BAR(B_Q), 0, &no_abort);
-      for (int it = issued - Lay::NS < 0 ? 0 : issued - Lay::NS; it < issued; ++it)
-        mbar_wait(BAR(B_FULL + it % Lay::NS), (it / Lay::NS) & 1, &no_abort);
+      for (int it = issued - ns < 0 ? 0 : issued - ns; it < issued; ++it)
+        mbar_wait(BAR(B_FULL + it % ns), (it / ns) & 1, &no_abort);
     }
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
       bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
+      int slot = 0, rnd = 0;   // of item 2j
       for (int j = 0; ok && j < n; ++j) {
         const int st = j & 1;
         // S buffer st last held S_{j-2}; the softmax is done with it once it
         // has published P_{j-2}.
         if (j >= 2 && !mbar_wait(BAR(B_PF + st), ((j - 2) >> 1) & 1, abort_flag)) break;
-        const int it = 2 * j;
-        const int slot = it % Lay::NS;
-        if (!mbar_wait(BAR(B_FULL + slot), (it / Lay::NS) & 1, abort_flag)) break;
+        if (!mbar_wait(BAR(B_FULL + slot), rnd & 1, abort_flag)) break;
         tc_fence_after();
         // S_j = Q K_j^T (both K-major): column block kb of the K tile sits at
         // kb * 8 KB; four K=16 steps of 32 B within each 128-byte row.
@@ -346,6 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         umma_commit(BAR(B_EMPTY + slot));
         umma_commit(BAR(B_SF + st));
+        if ((slot += 2) >= ns) {
+          slot -= ns;
+          ++rnd;
+        }
       }
       // No tensor-core work may be in flight when TMEM is released.
       umma_commit(BAR(B_DRAIN));
@@ -356,12 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // ------------------------------------------------------------ P V issuer
     if (lane == 0) {
       const uint32_t kIdescO = idesc_bf16_f32(kBM, DV, false, true);
+      int slot = 1, rnd = 0;   // of item 2j + 1 (ns >= 2)
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         if (!mbar_wait(BAR(B_PF + st), (j >> 1) & 1, abort_flag)) break;
-        const int it = 2 * j + 1;
-        const int slot = it % Lay::NS;
-        if (!mbar_wait(BAR(B_FULL + slot), (it / Lay::NS) & 1, abort_flag)) break;
+        if (!mbar_wait(BAR(B_FULL + slot), rnd & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t vt = sRing + slot * Lay::TILE;
 #pragma unroll
@@ -369,12 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           // A = P (K-major, 128 x 64 keys); B = V tile read MN-major: D runs
           // along the 128-byte rows, 64-column blocks 8 KB apart (LBO), 8-key
           // groups 1 KB apart (SBO), 16 keys = 2 KB per K step.
-          const uint64_t a = sdesc_sw128(sP + st * Lay::P_BYTES + kk * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(vt + kk * 16 * 128, 8192, 1024);
-          umma_bf16(tO, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tO, tP + st * (kBN / 2) + kk * 8, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(BAR(B_EMPTY + slot));
         umma_commit(BAR(B_PV + st));
+        if ((slot += 2) >= ns) {
+          slot -= ns;
+          ++rnd;
+        }
       }
       umma_commit(BAR(B_DRAIN));
       volatile int no_abort = 0;
@@ -468,12 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       // P buffer `st` was last read by P_{j-2} V_{j-2}.
       if (j >= 2 && !warp_wait(BAR(B_PV + st), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-      const uint32_t prow = sP + st * Lay::P_BYTES + row * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(prow + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                     pk[4 * c + 3]);
-      fence_proxy_async_smem();
+      tmem_st32(tP + st * (kBN / 2) + lane_off, reinterpret_cast<const float*>(pk));
       tc_fence_before();
       mbar_arrive(BAR(B_PF + st));
     }
@@ -708,16 +732,16 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
                         pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
 }
 
-template <int D>
+template <int D, int RING_KB>
 cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t s) {
-  using Lay = Layout<D>;
+  using Lay = Layout<D, RING_KB>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(attn_kernel<D, RING_KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Lay::ALLOC);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr_err = cudaFuncSetAttribute(attn_kernel<D, RING_KB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(m_tiles, prm.n_splits, Hkv * prm.dparts);
@@ -737,10 +761,10 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, attn_kernel<D>, prm);
+    e = cudaLaunchKernelEx(&cfg, attn_kernel<D, RING_KB>, prm);
     count_launch();
   } else {
-    e = launch_k(attn_kernel<D>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
+    e = launch_k(attn_kernel<D, RING_KB>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1 || prm.fused) return e;
@@ -756,21 +780,22 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
 // once, for c = 1..kMaxClusterSplits (index c); 0 where clusters of that size
 // cannot be scheduled.  Clusters live within one GPC, so this is not simply
 // SMs / c.  Queried once per head dimension.
-template <int D>
+template <int D, int RING_KB>
 const int* cluster_capacity() {
   static int cap[kMaxClusterSplits + 1];
   static bool done = false;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (done) return cap;
-  cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::ALLOC);
-  cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncSetAttribute(attn_kernel<D, RING_KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       Layout<D, RING_KB>::ALLOC);
+  cudaFuncSetAttribute(attn_kernel<D, RING_KB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cap[0] = 0;
   for (int c = 1; c <= kMaxClusterSplits; ++c) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, c, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Layout<D>::ALLOC;
+    cfg.dynamicSmemBytes = Layout<D, RING_KB>::ALLOC;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 1;
@@ -779,7 +804,7 @@ const int* cluster_capacity() {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    cap[c] = cudaOccupancyMaxActiveClusters(&n, attn_kernel<D>, &cfg) == cudaSuccess ? n : 0;
+    cap[c] = cudaOccupancyMaxActiveClusters(&n, attn_kernel<D, RING_KB>, &cfg) == cudaSuccess ? n : 0;
   }
   cudaGetLastError();
   done = true;
@@ -875,9 +900,9 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   // all fit on the device at once (one wave).
   const int* cap = nullptr;
   switch (a.D) {
-    case 64: cap = cluster_capacity<64>(); break;
-    case 128: cap = cluster_capacity<128>(); break;
-    case 256: cap = cluster_capacity<256>(); break;
+    case 64: cap = cluster_capacity<64, kRingDeepKB>(); break;   // the larger build: capacity it fits
+    case 128: cap = cluster_capacity<128, kRingDeepKB>(); break;
+    case 256: cap = cluster_capacity<256, kRingDeepKB>(); break;
     default: return cudaErrorInvalidValue;
   }
   const int units = m_total * a.Hkv;
@@ -915,14 +940,18 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   const bool fused = splits >= 2 && splits <= kMaxClusterSplits && cap[splits] >= 1;
   if (dparts != 1 && dparts != 2 && dparts != 4) return cudaErrorInvalidValue;
   if (a.D % (dparts * 64) != 0) return cudaErrorInvalidValue;
+  const bool deep = (t_max + splits - 1) / splits > kShallowTiles;
   prm.n_splits = splits;
   prm.dparts = dparts;
   prm.fused = fused ? 1 : 0;
   if (used_splits) *used_splits = splits;
   switch (a.D) {
-    case 64: return launch_one<64>(prm, m_total, a.Hkv, s);
-    case 128: return launch_one<128>(prm, m_total, a.Hkv, s);
-    case 256: return launch_one<256>(prm, m_total, a.Hkv, s);
+    case 64: return deep ? launch_one<64, kRingDeepKB>(prm, m_total, a.Hkv, s)
+                         : launch_one<64, kRingShallowKB>(prm, m_total, a.Hkv, s);
+    case 128: return deep ? launch_one<128, kRingDeepKB>(prm, m_total, a.Hkv, s)
+                          : launch_one<128, kRingShallowKB>(prm, m_total, a.Hkv, s);
+    case 256: return deep ? launch_one<256, kRingDeepKB>(prm, m_total, a.Hkv, s)
+                          : launch_one<256, kRingShallowKB>(prm, m_total, a.Hkv, s);
     default: return cudaErrorInvalidValue;
   }
 }
