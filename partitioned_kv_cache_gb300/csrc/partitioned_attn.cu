@@ -811,15 +811,17 @@ const int* cluster_capacity() {
   return cap;
 }
 
-// Relative cost of one launch in units of "one K tile plus one full V tile
-// streamed into an SM": tiles * (1 + 1/dparts) for the key loop, and with a
-// cluster merge the exchange of the partials through L2 (about 2.25 units for
-// a full-width partial) plus the merge's barrier and combine (about 2.5
-// units).  Fitted to timings of 2163- and 8448-key suffixes on GB300.
+// Relative cost of one launch, in units of about 0.7 us on GB300: each key
+// tile of the longest split costs 1 + 0.2/dparts (the K tile, the S tile
+// and the softmax chain are the same for every column share; only the V
+// bytes and the P V product shrink), and a cluster merge costs 3/dparts for
+// the partials' exchange through L2 plus 2.5 for its barrier and combine.
+// Fitted to timings of 2163- and 8448-key suffixes and the shared-cache batch
+// (12 x 2, 16 x 1 and 14 x 1 win there).
 double split_cost(int t_max, int splits, int dparts) {
   const int tiles = (t_max + splits - 1) / splits;
-  double c = tiles * (1.0 + 1.0 / dparts);
-  if (splits > 1) c += 2.25 / dparts + 2.5;
+  double c = tiles * (1.0 + 0.2 / dparts);
+  if (splits > 1) c += 3.0 / dparts + 2.5;
   return c;
 }
 
