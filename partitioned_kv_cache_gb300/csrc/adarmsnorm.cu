@@ -160,7 +160,27 @@ __global__ void __launch_bounds__(256) ada_gamma_kernel(
 #pragma unroll
     for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
     const __nv_bfloat16* wr = W1s + static_cast<size_t>(j) * cond_dim;
-    for (int e = 0; e < cond_dim; ++e) {
+    int e0 = 0;
+    if ((cond_dim & 7) == 0 && (reinterpret_cast<uintptr_t>(W1s) & 15) == 0) {
+      // 16-byte rows: 8 weights per load, four loads in flight
+      const uint4* w4 = reinterpret_cast<const uint4*>(wr);
+      for (; e0 + 32 <= cond_dim; e0 += 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = w4[e0 / 8 + u];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float w[8];
+          unpack8(v[u], w);
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+#pragma unroll
+            for (int k = 0; k < kMaxCond; ++k)
+              if (k < n_cond) acc[k] = fmaf(w[x], c[k * cond_dim + e0 + 8 * u + x], acc[k]);
+        }
+      }
+    }
+    for (int e = e0; e < cond_dim; ++e) {
       const float w = __bfloat162float(wr[e]);
 #pragma unroll
       for (int k = 0; k < kMaxCond; ++k)
@@ -190,6 +210,7 @@ __global__ void __launch_bounds__(256) ada_gamma_kernel(
   for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
   const int ir = i < d ? i : d - 1;   // rows past d compute a duplicate and are not stored
   const uint2* wr = reinterpret_cast<const uint2*>(W2s + static_cast<size_t>(ir) * hidden);
+#pragma unroll 8
   for (int t = 0; t < hidden / 16; ++t) {
     const int j = 16 * t + 4 * q;
     const uint2 wv = wr[j >> 2];
