@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int nt_win = (win_len + kBN - 1) / kBN;
   const int nt_dyn = (sg.n_priv + kBN - 1) / kBN;
   const int T = nt_pin + nt_win + nt_dyn;
-  const int t0 = static_cast<int>(static_cast<long long>(split) * T / p.n_splits);
-  const int t1 = static_cast<int>(static_cast<long long>(split + 1) * T / p.n_splits);
+  const int t0 = static_cast<int>(static_cast<unsigned>(split * T) / static_cast<unsigned>(p.n_splits));
+  const int t1 = static_cast<int>(static_cast<unsigned>((split + 1) * T) / static_cast<unsigned>(p.n_splits));
   const int n = t1 - t0;
 
   const uint32_t tmem = *tmem_slot;
