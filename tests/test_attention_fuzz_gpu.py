@@ -1,0 +1,77 @@
+"""Seeded random shapes for partitioned attention against the fp64 oracle.
+
+"Reflex: Real-Time VLA Control through Streaming Inference", §III Eq. (1):
+every suffix query attends with one softmax over [pinned; window; dynamic].
+Each case draws a head dimension, a grouping of query heads over K/V heads,
+pinned / window / suffix sizes (including empty and ragged regions and a
+wrapped window), a number of pushes, and a forced or automatic partition of
+the key sequence, then compares every output element with the oracle.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention as OA
+from oracle.pipeline import OracleStream
+from partitioned_kv_cache_gb300 import workload as W
+from tests._util import check_attention, dev, ensure_built, host64
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 48
+
+
+@pytest.fixture(scope="module")
+def rx():
+    ensure_built()
+    from partitioned_kv_cache_gb300 import rx as m
+    return m
+
+
+def _case(i):
+    g = np.random.default_rng(1000 + i)
+    D = int(g.choice([64, 128, 256]))
+    Hkv = int(g.choice([1, 1, 2, 4]))
+    G = int(g.choice([1, 2, 4, 8, 16]))
+    P = int(g.choice([0, 1, 37, 64, 150]))
+    N = int(g.integers(1, 6))
+    F = int(g.choice([1, 17, 64, 100, 128]))
+    S = int(g.integers(1, 70))
+    if P == 0 and S == 0:
+        S = 1
+    pushes = int(g.integers(0, N + 4))
+    splits = int(g.choice([0, 0, 1, 3, 7, 16, 20]))
+    dparts = int(g.choice([0, 0, 1, 2, 4]))
+    if dparts and D // dparts < 64:
+        dparts = 0
+    return dict(D=D, Hkv=Hkv, Hq=G * Hkv, P=P, N=N, F=F, S=S, pushes=pushes, splits=splits, dparts=dparts)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_shape(rx, i):
+    c = _case(i)
+    wl = W.Workload("fuzz%d" % i, L=2, Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], P=c["P"], N=c["N"], F=c["F"],
+                    S=c["S"], steps=1, ticks=1, d_model=128, emb_dim=16, state_dim=16, hidden=64)
+    seed = 77 + i
+    cache = rx.Cache(wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S)
+    if c["P"] > 0:
+        pk, pv = W.pinned_kv(wl, seed)
+        cache.pin_prefix(dev(pk), dev(pv))
+    cache.set_attn_splits(min(c["splits"], 64))
+    cache.set_attn_dparts(c["dparts"])
+    ost = OracleStream(wl, seed)
+    for t in range(c["pushes"]):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    f = W.bf16_bits_to_f64
+    for layer in range(wl.L):
+        q, kd, vd = W.suffix_qkv(wl, seed, max(c["pushes"] - 1, 0), 0, layer)
+        got = host64(cache.attend_suffix(layer, dev(q), dev(kd), dev(vd)))
+        ks, vs = ost.regions(layer, f(kd), f(vd))
+        ref = OA.partitioned_attention(f(q), ks, vs)
+        # Few keys make outputs non-averages: bound by the bf16 roundings of P
+        # and the output, 2^-8 * max|V| (see the edge-shape test).
+        vmax = max(float(np.abs(v).max()) for v in vs if v.size)
+        check_attention(got, ref, max(1.0, 2.0 ** -8 * vmax / 1e-2))
+    assert cache.check_device_error() == 0
+    cache.close()
