@@ -75,3 +75,61 @@ def test_random_shape(rx, i):
         check_attention(got, ref, max(1.0, 2.0 ** -8 * vmax / 1e-2))
     assert cache.check_device_error() == 0
     cache.close()
+
+
+N_BATCH_CASES = 16
+
+
+@pytest.mark.parametrize("i", range(N_BATCH_CASES))
+def test_random_batch(rx, i):
+    """"OxyGen ...", §"Core method": random language batches (streams, query
+    tokens per stream, tail capacities and lengths, with or without the action
+    suffix in the same launch) over a shared cache of random shape."""
+    import torch
+    g = np.random.default_rng(2000 + i)
+    D = int(g.choice([64, 128, 256]))
+    Hkv = int(g.choice([1, 1, 2]))
+    Hq = int(g.choice([1, 2, 4, 8])) * Hkv
+    B, T = int(g.integers(1, 21)), int(g.integers(1, 4))
+    tail_cap = int(g.integers(1, 41))
+    S = int(g.integers(1, 60))
+    wl = W.Workload("bfuzz%d" % i, L=1, Hq=Hq, Hkv=Hkv, D=D, P=int(g.choice([0, 20, 64])), N=int(g.integers(1, 4)),
+                    F=int(g.choice([17, 64])), S=S, steps=1, ticks=1, d_model=128, emb_dim=16, state_dim=16,
+                    hidden=64, n_lang=B, tail_max=tail_cap, tail_cap=tail_cap)
+    seed = 300 + i
+    cache = rx.Cache(wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S, wl.tail_cap, B * T)
+    if wl.P > 0:
+        pk, pv = W.pinned_kv(wl, seed)
+        cache.pin_prefix(dev(pk), dev(pv))
+    ost = OracleStream(wl, seed)
+    for t in range(int(g.integers(0, wl.N + 2))):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    f = W.bf16_bits_to_f64
+    q = W.to_bf16_bits(g.standard_normal((B, T, Hq, D), dtype=np.float32))
+    tk = W.to_bf16_bits(g.standard_normal((B, tail_cap, Hkv, D), dtype=np.float32))
+    tv = W.to_bf16_bits(g.standard_normal((B, tail_cap, Hkv, D), dtype=np.float32))
+    ln = g.integers(0, tail_cap + 1, size=B).astype(np.int32)
+    if wl.P == 0 and len(ost.window.window()) == 0:
+        ln = np.maximum(ln, 1)   # every stream needs at least one key
+    lang = (dev(q), dev(tk), dev(tv), torch.from_numpy(ln).cuda())
+    with_action = bool(g.integers(0, 2))
+    action = None
+    if with_action:
+        aq, akd, avd = W.suffix_qkv(wl, seed, 0, 0, 0)
+        action = (dev(aq), dev(akd), dev(avd))
+    oa, ol = cache.attend_batch(0, action, lang)
+    ks, vs = ost.regions(0, np.zeros((0, Hkv, D)), np.zeros((0, Hkv, D)))
+    reqs = [(f(q[b]), f(tk[b, :ln[b]]), f(tv[b, :ln[b]])) for b in range(B)]
+    refs = OA.shared_cache_attention(ks[:-1], vs[:-1], reqs)
+    got = host64(ol)
+    vmax = max([float(np.abs(v).max()) for v in vs[:-1] if v.size] + [float(np.abs(f(tv)).max())])
+    for b, ref in enumerate(refs):
+        check_attention(got[b], ref, max(1.0, 2.0 ** -8 * vmax / 1e-2))
+    if with_action:
+        aks, avs = ost.regions(0, f(akd), f(avd))
+        amax = max(float(np.abs(v).max()) for v in avs if v.size)
+        check_attention(host64(oa), OA.partitioned_attention(f(aq), aks, avs), max(1.0, 2.0 ** -8 * amax / 1e-2))
+    assert cache.check_device_error() == 0
+    cache.close()
