@@ -182,8 +182,17 @@ __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constan
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(base), "r"(bytes)
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the tile is written
-    asm volatile("fence.proxy.async.global;" ::: "memory");    // ... and ordered before what follows
+    if (a.slots > a.N) {
+      // Spare-slot ring: attention may run concurrently and reads the state
+      // as soon as it is published, so the tile must be written first.
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    } else {
+      // Otherwise every reader is ordered after this kernel, whose completion
+      // makes the tile visible: only the shared-memory source must be read
+      // before this CTA exits.
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
   } else {
     // the copy may still land in shared memory: wait for it (bounded) before exiting
     volatile int no_abort = 0;
