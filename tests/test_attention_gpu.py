@@ -223,3 +223,34 @@ def test_argument_errors(rx):
     with pytest.raises(rx.RxError):
         cache.set_attn_splits(10 ** 6)
     cache.close()
+
+
+def test_two_caches_on_two_streams_run_concurrently(rx):
+    """Each cache owns its exchange workspace: attention on two caches issued
+    alternately on two CUDA streams (so their kernels overlap) gives each
+    cache's own result."""
+    import torch
+    wl = W.WORKLOADS["c2"]
+    caches, osts, streams = [], [], [torch.cuda.Stream(), torch.cuda.Stream()]
+    for seed in (11, 12):
+        c = _make(rx, wl, seed)
+        o = OracleStream(wl, seed)
+        for t in range(wl.N + 1):
+            fk, fv = W.frame_kv(wl, seed, t)
+            c.push_frame(dev(fk), dev(fv))
+            o.push(t)
+        caches.append(c)
+        osts.append(o)
+    torch.cuda.synchronize()
+    inputs = [[tuple(dev(a) for a in W.suffix_qkv(wl, 11 + i, wl.N, k, 0)) for k in range(6)] for i in range(2)]
+    outs = [[None] * 6 for _ in range(2)]
+    for k in range(6):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                outs[i][k] = caches[i].attend_suffix(0, *inputs[i][k])
+    torch.cuda.synchronize()
+    for i in range(2):
+        for k in range(6):
+            check_attention(host64(outs[i][k]), _oracle_attend(osts[i], wl, 11 + i, wl.N, k, 0))
+        assert caches[i].check_device_error() == 0
+        caches[i].close()
