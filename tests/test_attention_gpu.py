@@ -254,3 +254,25 @@ def test_two_caches_on_two_streams_run_concurrently(rx):
             check_attention(host64(outs[i][k]), _oracle_attend(osts[i], wl, 11 + i, wl.N, k, 0))
         assert caches[i].check_device_error() == 0
         caches[i].close()
+
+
+@pytest.mark.parametrize("splits", [0, 16, 40])
+def test_long_suffix_many_query_tiles(rx, splits):
+    """A 1024-token suffix (8192 query rows, 64 query tiles): more clusters
+    than fit at once (several waves), or the global-memory merge with 40
+    splits.  Sampled tokens are checked against the oracle."""
+    wl = W.Workload("long-suffix", L=1, Hq=8, Hkv=1, D=256, P=48, N=4, F=256, S=1024, steps=1, ticks=1,
+                    d_model=128, emb_dim=16, state_dim=16, hidden=64)
+    seed = 13
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(splits)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    tokens = [0, 1, 127, 128, 500, 511, 512, 1000, 1022, 1023]
+    got = host64(_attend(cache, wl, seed, wl.N, 0, 0))[tokens]
+    check_attention(got, _oracle_attend(ost, wl, seed, wl.N, 0, 0, tokens=tokens))
+    assert cache.check_device_error() == 0
+    cache.close()
