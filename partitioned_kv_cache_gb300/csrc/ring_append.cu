@@ -158,6 +158,24 @@ struct PackTma {
   int Hkv, D, T, tok0, F, N, slots;
 };
 
+// The last of the grid's CTAs to arrive publishes the advanced state.  acq_rel:
+// each CTA's read of the old state is ordered before its arrival, and the
+// publisher's stores after every arrival.
+__device__ __forceinline__ void arrive_and_publish(DevState* st, unsigned int total, int head,
+                                                   int valid, int N, int slots) {
+  unsigned int prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+               : "=r"(prev)
+               : "l"(&st->append_arrivals)
+               : "memory");
+  if (prev == total - 1) {
+    publish_ring_state(st, head + 1 == slots ? 0 : head + 1, valid < N ? valid + 1 : N);
+    st->pushes += 1;
+    st->append_arrivals = 0;
+    __threadfence();
+  }
+}
+
 __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constant__ PackTma a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // swizzle atoms are 1 KB
@@ -165,16 +183,26 @@ __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constan
   grid_dependency_wait();
   grid_launch_dependents();
   if (threadIdx.x != 0) return;
-  int head = 0, valid = 0;
-  if (a.st) load_ring_state(a.st, &head, &valid);
-  const int base_tok = a.st ? head * a.F : a.tok0;   // a multiple of 64 (host-checked)
   const int l = blockIdx.y / a.Hkv, g = blockIdx.y % a.Hkv, kv = blockIdx.z;
   const uint32_t bytes = static_cast<uint32_t>(tile_bytes(a.D));
+  // The source boxes do not depend on the ring state: issue them first and
+  // read the state while they are in flight.
   mbar_init(bar, 1);
   fence_barrier_init();
   mbar_arrive_expect_tx(bar, bytes);
   for (int kb = 0; kb < a.D / 64; ++kb)
     tma_load_4d(base + kb * 8192, &a.tm[kv], kb * 64, g, blockIdx.x * kTileTok, l, bar);
+  int head = 0, valid = 0;
+  if (a.st) load_ring_state(a.st, &head, &valid);
+  const bool spare = a.slots > a.N;
+  const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+  if (a.st && !spare) {
+    // Without a spare slot every reader of the state and of the slot is
+    // ordered after this kernel's completion, which makes the tile visible:
+    // the publish only has to wait until every CTA has read the old state.
+    arrive_and_publish(a.st, total, head, valid, a.N, a.slots);
+  }
+  const int base_tok = a.st ? head * a.F : a.tok0;   // a multiple of 64 (host-checked)
   volatile int gave_up = 0;
   const bool ok = mbar_wait(bar, 0, &gave_up);
   if (ok) {
@@ -182,15 +210,13 @@ __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constan
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(base), "r"(bytes)
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    if (a.slots > a.N) {
+    if (spare) {
       // Spare-slot ring: attention may run concurrently and reads the state
       // as soon as it is published, so the tile must be written first.
       asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");
     } else {
-      // Otherwise every reader is ordered after this kernel, whose completion
-      // makes the tile visible: only the shared-memory source must be read
-      // before this CTA exits.
+      // Only the shared-memory source must be read before this CTA exits.
       asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
   } else {
@@ -199,17 +225,9 @@ __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constan
     mbar_wait(bar, 0, &no_abort);
     if (a.st) atomicOr(&a.st->err, kErrAppendTimeout);
   }
-  if (!a.st) return;
-  __threadfence();
-  const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
-  const unsigned int prev = atomicAdd(&a.st->append_arrivals, 1u);
-  if (prev == total - 1) {
-    // Every CTA wrote its tile and fenced before arriving: publish.
+  if (a.st && spare) {
     __threadfence();
-    publish_ring_state(a.st, head + 1 == a.slots ? 0 : head + 1, valid < a.N ? valid + 1 : a.N);
-    a.st->pushes += 1;
-    a.st->append_arrivals = 0;
-    __threadfence();
+    arrive_and_publish(a.st, total, head, valid, a.N, a.slots);
   }
 }
 
