@@ -1,0 +1,94 @@
+"""A stream tick captured once as a CUDA graph and replayed tick after tick.
+
+"Reflex: Real-Time VLA Control through Streaming Inference", §III "System
+architecture" (each tick enqueues the newest frame and evicts the oldest) and
+Eq. (1).  The ring state lives on the device and the append kernel advances
+it, so replaying one captured {push, attention over every layer and step}
+must walk the window exactly as eager calls do.  After every replay each
+output is compared with the oracle and layer 0's window with the oracle's
+frames, bit for bit.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention as OA
+from oracle.pipeline import OracleStream
+from partitioned_kv_cache_gb300 import workload as W
+from tests._util import check_attention, dev, ensure_built, host64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rx():
+    ensure_built()
+    from partitioned_kv_cache_gb300 import rx as m
+    return m
+
+
+@pytest.mark.parametrize("spare", [0, 1])
+def test_replayed_tick_matches_the_oracle(rx, spare):
+    import torch
+    wl = W.Workload("graph-3L", L=3, Hq=8, Hkv=1, D=256, P=48, N=4, F=256, S=51, steps=2, ticks=1,
+                    d_model=128, emb_dim=16, state_dim=16, hidden=64)
+    seed = 21
+    f = W.bf16_bits_to_f64
+    cache = rx.Cache(wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S, spare_slot=spare)
+    pk, pv = W.pinned_kv(wl, seed)
+    cache.pin_prefix(dev(pk), dev(pv))
+    ost = OracleStream(wl, seed)
+
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    fk = torch.empty((wl.L, wl.F, wl.Hkv, wl.D), **bf)
+    fv = torch.empty_like(fk)
+    q = torch.empty((wl.steps, wl.L, wl.S, wl.Hq, wl.D), **bf)
+    kd = torch.empty((wl.steps, wl.L, wl.S, wl.Hkv, wl.D), **bf)
+    vd = torch.empty_like(kd)
+    o = torch.empty_like(q)
+    s = torch.cuda.Stream()
+
+    def load(t):   # tick t's inputs into the captured buffers, ordered on s
+        a, b = W.frame_kv(wl, seed, t)
+        fk.copy_(dev(a))
+        fv.copy_(dev(b))
+        for k in range(wl.steps):
+            for l in range(wl.L):
+                qq, kk, vv = W.suffix_qkv(wl, seed, t, k, l)
+                q[k, l].copy_(dev(qq))
+                kd[k, l].copy_(dev(kk))
+                vd[k, l].copy_(dev(vv))
+
+    def tick():
+        cache.push_frame(fk, fv)
+        for k in range(wl.steps):
+            for l in range(wl.L):
+                cache.attend_suffix(l, q[k, l], kd[k, l], vd[k, l], out=o[k, l])
+
+    def check(t):
+        ost.push(t)
+        for k in range(wl.steps):
+            for l in range(wl.L):
+                qq, kk, vv = (f(a) for a in W.suffix_qkv(wl, seed, t, k, l))
+                ks, vs = ost.regions(l, kk, vv)
+                check_attention(host64(o[k, l]), OA.partitioned_attention(qq, ks, vs))
+        kw, _ = cache.export_window(0)
+        want = np.concatenate([fr[1][0] for fr in ost.window.window()])
+        np.testing.assert_array_equal(host64(kw), want)
+
+    with torch.cuda.stream(s):   # tick 0 eagerly (first launches set kernel attributes)
+        load(0)
+        tick()
+    torch.cuda.synchronize()
+    check(0)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        tick()
+    for t in range(1, 2 * wl.N + 2):
+        with torch.cuda.stream(s):
+            load(t)
+            gr.replay()
+        torch.cuda.synchronize()
+        check(t)
+    assert cache.debug_window() is not None
+    assert cache.check_device_error() == 0
+    cache.close()
