@@ -67,3 +67,41 @@ def test_zero_rows_is_a_noop(rx):
     x = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     g = torch.ones(64, device="cuda")
     assert rx.adarmsnorm(x, g, 1e-6).shape == (0, 64)
+
+
+@pytest.mark.parametrize("d,hidden,emb,state_dim,n_cond,wscale", [
+    (1000, 80, 16, 16, 16, 1.0),     # ragged 128-row tile, hidden not a multiple of 64, 16 vectors
+    (136, 2048, 6, 5, 1, 1.0),       # widest hidden; conditioning width 11 (not a multiple of 8)
+    (8, 16, 2, 0, 5, 1.0),           # smallest shapes, no state
+    (256, 512, 16, 16, 10, 50.0),    # weights ~N(0, 1): gamma - 1 of order 100
+])
+def test_gamma_shapes_and_scales(rx, d, hidden, emb, state_dim, n_cond, wscale):
+    """Eq. (2)'s gamma MLP over the edge shapes of the kernel.  Bound: the
+    error of an fp32 evaluation with the hidden activation carried to ~2^-17
+    (two bf16 parts), 4e-5 x sum_j |W2_ij h_j| + |b2_i| per element."""
+    import torch
+    wl = W.Workload("gamma-shape", L=1, Hq=1, Hkv=1, D=64, P=0, N=1, F=1, S=1, steps=n_cond,
+                    ticks=1, d_model=d, emb_dim=emb, state_dim=state_dim, hidden=hidden)
+    seed = 31
+    ws = []
+    for site in range(2):
+        w = W.mlp_weights(wl, seed, 0, site)
+        if wscale != 1.0:
+            w = tuple(W.to_bf16_bits((W.bf16_bits_to_f64(a) * wscale).astype(np.float32)) for a in w)
+        ws.append(w)
+    W1, b1, W2, b2 = (dev(np.stack([w[j] for w in ws])) for j in range(4))
+    t = torch.from_numpy(W.timesteps(wl)).cuda()
+    st = W.robot_state(wl, seed, 0)
+    state = torch.from_numpy(np.repeat(st[None], n_cond, axis=0).reshape(n_cond, state_dim)).cuda()
+    gamma = rx.ada_gamma(t, state, W1, b1, W2, b2, emb).cpu().numpy()
+    assert np.all(np.isfinite(gamma))
+    for s_i, w in enumerate(ws):
+        w64 = [W.bf16_bits_to_f64(a) for a in w]
+        for k, tk in enumerate(W.timesteps(wl)):
+            c = OA.conditioning(float(tk), st, emb)
+            ref = OA.gamma_mlp(c, *w64)
+            h = OA.silu(w64[0] @ c + w64[1])
+            bound = 4e-5 * (np.abs(w64[2]) @ np.abs(h) + np.abs(w64[3])) + 1e-7
+            err = np.abs(gamma[s_i, k] - ref)
+            assert np.all(err <= bound), "set %d vector %d: worst err/bound %.2f" % (
+                s_i, k, float(np.max(err / bound)))
