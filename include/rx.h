@@ -228,9 +228,14 @@ rx_status rx_restore(rx_cache_t cache, const void* src, void* stream);
  * t: fp32 [n_cond]; state: fp32 [n_cond][state_dim];
  * W1: bf16 [n_sets][hidden][emb_dim+state_dim]; b1: bf16 [n_sets][hidden];
  * W2: bf16 [n_sets][d][hidden]; b2: bf16 [n_sets][d];
- * gamma: fp32 [n_sets][n_cond][d] (output).  bf16 weights, fp32 arithmetic.
+ * gamma: fp32 [n_sets][n_cond][d] (output).  bf16 weights, fp32 arithmetic;
+ * the second layer runs on the tensor cores with SiLU(...) split into two
+ * bf16 parts (~16 bits kept) and an fp32 accumulator.  W2 must be 16-byte
+ * aligned.  A device-side timeout (a copy that never lands) writes NaN into
+ * the affected outputs.
  * Limits: 1 <= n_cond <= 16, emb_dim even, hidden % 16 == 0 and <= 2048,
- * d % 8 == 0.
+ * d % 8 == 0; RX_ERR_CUDA if the conditioning vectors and H do not fit in
+ * shared memory (emb_dim + state_dim of several hundred with hidden 2048).
  * Errors: RX_ERR_ARG, RX_ERR_CUDA. */
 rx_status rx_ada_gamma(const float* t, const float* state, int n_cond,
                        int emb_dim, int state_dim, const void* W1,
