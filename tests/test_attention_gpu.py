@@ -276,3 +276,54 @@ def test_long_suffix_many_query_tiles(rx, splits):
     check_attention(got, _oracle_attend(ost, wl, seed, wl.N, 0, 0, tokens=tokens))
     assert cache.check_device_error() == 0
     cache.close()
+
+
+@pytest.mark.parametrize("splits", [1, 2, 0])
+def test_running_maximum_rescale(rx, splits):
+    """Online softmax with a maximum that jumps by more than 2^8 in the last
+    key tile ("Reflex ...", §III Eq. (1): one softmax over all regions).  320
+    keys score near 0 and one dynamic key scores ~2^10.6 above them, so the O
+    accumulated over the first five tiles must be rescaled in place.  The old
+    keys carry ~15% of the weight with values near +1 and the jumping key's
+    value is -1, so a wrong rescale factor moves the output visibly.  One split
+    walks every tile in order.  The output is of order 1, so the bound is the
+    rounding of the path, not the unit-scale tolerance: bf16 output rounding
+    (2^-9 |o|) plus bf16 P in the P V product (2^-9 max|v|), doubled."""
+    D, G, S, P, N, F = 64, 8, 51, 64, 4, 64
+    rng = np.random.default_rng(77)
+    u = np.zeros(D, np.float32)
+    u[3] = 1.0
+    bits = lambda a: W.to_bf16_bits(np.ascontiguousarray(a, dtype=np.float32))
+    near_one = lambda *shape: 1.0 + 0.1 * rng.standard_normal(shape)
+    q = bits(np.broadcast_to(4.0 * u, (S, G, D)))
+    pin_k = bits(rng.standard_normal((1, P, 1, D)) * 0.1)
+    pin_v = bits(near_one(1, P, 1, D))
+    frames = [(bits(rng.standard_normal((1, F, 1, D)) * 0.1), bits(near_one(1, F, 1, D))) for _ in range(N)]
+    kd = rng.standard_normal((S, 1, D)).astype(np.float32) * 0.1
+    kd[7, 0] = 15.0 * u
+    vd = (0.1 * rng.standard_normal((S, 1, D))).astype(np.float32)
+    vd[7, 0] = -1.0
+    kd, vd = bits(kd), bits(vd)
+    cache = rx.Cache(1, G, 1, D, P, N, F, S)
+    cache.pin_prefix(dev(pin_k), dev(pin_v))
+    for fk, fv in frames:
+        cache.push_frame(dev(fk), dev(fv))
+    cache.set_attn_splits(splits)
+    got = host64(cache.attend_suffix(0, dev(q), dev(kd), dev(vd)))
+    f = W.bf16_bits_to_f64
+    ks = [f(pin_k)[0]] + [f(fk)[0] for fk, _ in frames] + [f(kd)]
+    vs = [f(pin_v)[0]] + [f(fv)[0] for _, fv in frames] + [f(vd)]
+    ref = OA.partitioned_attention(f(q), ks, vs)
+    # the jump really is above the rescale threshold, and the old keys matter
+    sc = np.einsum("d,kd->k", f(q)[0, 0], np.concatenate([k[:, 0] for k in ks])) / np.sqrt(D) / np.log(2)
+    spike = len(sc) - S + 7
+    assert sc[spike] - np.max(np.delete(sc, spike)) > 9.0
+    w_old = np.exp2(sc[:len(sc) - S] - sc[spike]).sum() / np.exp2(sc - sc[spike]).sum()
+    assert w_old > 0.1
+    assert np.all(np.isfinite(got))
+    vmax = max(float(np.abs(v).max()) for v in vs)
+    bound = 2.0 ** -8 * (np.abs(ref) + vmax)
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), "worst err / bound %.2f" % float(np.max(err / bound))
+    assert cache.check_device_error() == 0
+    cache.close()
