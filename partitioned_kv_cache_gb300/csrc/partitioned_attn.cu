@@ -817,7 +817,9 @@ const int* cluster_capacity() {
 // bytes and the P V product shrink), and a cluster merge costs 3/dparts for
 // the partials' exchange through L2 plus 2.5 for its barrier and combine.
 // Fitted to timings of 2163- and 8448-key suffixes and the shared-cache batch
-// (12 x 2, 16 x 1 and 14 x 1 win there).
+// (12 x 2, 16 x 1 and 16 x 1 win there).  Ties go to more splits: the longest
+// split is as long, but the average one is shorter (8448 keys: 16 x 1 is
+// 0.4 us faster than 15 x 1; the batch: 16 x 1 0.3 us faster than 14 x 1).
 double split_cost(int t_max, int splits, int dparts) {
   const int tiles = (t_max + splits - 1) / splits;
   double c = tiles * (1.0 + 0.2 / dparts);
@@ -926,7 +928,7 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
         if (dparts > 0 && dp != dparts) continue;
         if (a.D / dp < 64 || !fits(sp, dp)) continue;
         const double c = split_cost(t_max, sp, dp);
-        if (c < best - 1e-9) {
+        if (c < best - 1e-9 || (c < best + 1e-9 && sp > bs)) {
           best = c;
           bs = sp;
           bd = dp;
