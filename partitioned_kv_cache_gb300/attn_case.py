@@ -12,6 +12,14 @@ norm sites x K steps) a few times, each on its own weight set:
 
     python -m partitioned_kv_cache_gb300.attn_case --workload c3 --op gamma --calls 4
 
+--op push pushes distinct frames into a store of the workload's layers
+(--frame-mult scales the frame's tokens), and --op norm runs AdaRMSNorm over
+--rows rows of the model width (default: the suffix), each call on its own
+input:
+
+    python -m partitioned_kv_cache_gb300.attn_case --workload c3 --op push --layers 18 --calls 6
+    python -m partitioned_kv_cache_gb300.attn_case --workload c3 --op norm --calls 6
+
 Inputs are seeded random bf16; nothing is checked here (the tests compare with
 the oracle).
 """
@@ -28,7 +36,9 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", default="c3", choices=sorted(W.WORKLOADS))
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--calls", type=int, default=6)
-    ap.add_argument("--op", default="attention", choices=["attention", "gamma"])
+    ap.add_argument("--op", default="attention", choices=["attention", "gamma", "push", "norm"])
+    ap.add_argument("--frame-mult", type=int, default=1)
+    ap.add_argument("--rows", type=int, default=0)
     a = ap.parse_args(argv)
     wl = W.WORKLOADS[a.workload]
     L = max(1, min(a.layers, wl.L))
@@ -51,6 +61,29 @@ def main(argv=None) -> None:
         if not bool(torch.isfinite(out).all()):
             raise SystemExit("non-finite gamma")
         print("%s: %d gamma launches of %d sets x %d steps" % (wl.name, a.calls, n_sets, wl.steps))
+        return
+
+    if a.op == "push":
+        F = wl.F * max(1, a.frame_mult)
+        cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, F, wl.S)
+        for _ in range(a.calls):
+            cache.push_frame(r(L, F, wl.Hkv, wl.D), r(L, F, wl.Hkv, wl.D))
+        torch.cuda.synchronize()
+        if cache.check_device_error() != 0:
+            raise SystemExit("a kernel reported a device-side timeout")
+        cache.close()
+        print("%s: %d pushes of %d tokens x %d layers" % (wl.name, a.calls, F, L))
+        return
+    if a.op == "norm":
+        rows = a.rows if a.rows > 0 else wl.S
+        gamma = (1.0 + 0.1 * torch.randn(wl.d_model, generator=g, device="cuda")).float()
+        ys = []
+        for _ in range(a.calls):
+            ys.append(rx.adarmsnorm(r(rows, wl.d_model), gamma, wl.eps))
+        torch.cuda.synchronize()
+        if not all(bool(torch.isfinite(y.float()).all()) for y in ys):
+            raise SystemExit("non-finite norm output")
+        print("%s: %d norms of %d x %d" % (wl.name, a.calls, rows, wl.d_model))
         return
 
     cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S)
