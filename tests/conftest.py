@@ -13,8 +13,8 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests skip (not fail) on a machine without a GPU so that `-m "not gpu"`
-    # and plain collection both work here; on a GPU machine they run.
+    # GPU tests skip (not fail) on a machine without a CUDA device, so that
+    # `-m "not gpu"` and plain collection work anywhere; with a device they run.
     try:
         import torch
         has_gpu = torch.cuda.is_available()
