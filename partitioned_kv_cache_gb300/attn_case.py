@@ -7,6 +7,8 @@ one launch of the attention kernel can be captured in isolation:
 
     python -m partitioned_kv_cache_gb300.attn_case --workload c4 --layers 2 --calls 6
 
+(--suffix replaces the workload's suffix length, e.g. 1024 query tokens.)
+
 --op gamma issues the gamma-MLP launch of one tick of the workload (all 2L
 norm sites x K steps) a few times, each on its own weight set:
 
@@ -39,6 +41,7 @@ def main(argv=None) -> None:
     ap.add_argument("--op", default="attention", choices=["attention", "gamma", "push", "norm"])
     ap.add_argument("--frame-mult", type=int, default=1)
     ap.add_argument("--rows", type=int, default=0)
+    ap.add_argument("--suffix", type=int, default=0)
     a = ap.parse_args(argv)
     wl = W.WORKLOADS[a.workload]
     L = max(1, min(a.layers, wl.L))
@@ -86,13 +89,14 @@ def main(argv=None) -> None:
         print("%s: %d norms of %d x %d" % (wl.name, a.calls, rows, wl.d_model))
         return
 
-    cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S)
+    S = a.suffix if a.suffix > 0 else wl.S
+    cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, S)
     cache.pin_prefix(r(L, wl.P, wl.Hkv, wl.D), r(L, wl.P, wl.Hkv, wl.D))
     for _ in range(wl.N):
         cache.push_frame(r(L, wl.F, wl.Hkv, wl.D), r(L, wl.F, wl.Hkv, wl.D))
-    q = r(wl.S, wl.Hq, wl.D)
-    kd = r(wl.S, wl.Hkv, wl.D)
-    vd = r(wl.S, wl.Hkv, wl.D)
+    q = r(S, wl.Hq, wl.D)
+    kd = r(S, wl.Hkv, wl.D)
+    vd = r(S, wl.Hkv, wl.D)
     o = torch.empty_like(q)
     for i in range(a.calls):
         cache.attend_suffix(i % L, q, kd, vd, out=o)
