@@ -278,6 +278,28 @@ def test_long_suffix_many_query_tiles(rx, splits):
     cache.close()
 
 
+def test_2048_token_suffix_one_split_per_tile(rx):
+    """A 2048-token suffix over an 8-frame window (16384 query rows, 128 query
+    tiles, 4160 keys): the automatic partition gives every query tile one CTA
+    that walks all 65 key tiles and writes the output itself (no merge), the
+    longest key loop the kernel runs.  Sampled tokens against the oracle."""
+    wl = W.Workload("suffix-2048", L=1, Hq=8, Hkv=1, D=256, P=64, N=8, F=256, S=2048, steps=1, ticks=1,
+                    d_model=128, emb_dim=16, state_dim=16, hidden=64)
+    seed = 17
+    cache = _make(rx, wl, seed)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 2):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    tokens = [0, 15, 16, 1023, 1024, 2031, 2047]
+    assert max(tokens) < wl.S
+    got = host64(_attend(cache, wl, seed, wl.N + 1, 0, 0))[tokens]
+    check_attention(got, _oracle_attend(ost, wl, seed, wl.N + 1, 0, 0, tokens=tokens))
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
 @pytest.mark.parametrize("splits", [1, 2, 0])
 def test_running_maximum_rescale(rx, splits):
     """Online softmax with a maximum that jumps by more than 2^8 in the last
