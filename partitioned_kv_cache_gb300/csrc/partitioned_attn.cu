@@ -18,6 +18,10 @@
 //     caller's dynamic K/V (and any untiled region) come in by TMA boxes that
 //     produce the same layout.  K and V tiles stream through a ring of slots;
 //     a K slot is released once Q K^T has read it, a V slot once P V has.
+//     Short key loops use one ring with K and V alternating; longer ones (the
+//     deeper build) keep K and V in separate rings, each filled by its own
+//     producer lane, so that a K load never waits for the P V that frees a
+//     V slot.
 //   * S = Q K^T and O += P V run on tcgen05 with both accumulators in TMEM
 //     (O: D columns; S: two 64-column buffers).  One thread per row does the
 //     online softmax in the exp2 domain and writes P (bf16) back to TMEM (two
@@ -63,7 +67,8 @@ constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a 
 // Shared memory for the K/V ring.  Two builds of the kernel: 128 KB for key
 // loops of at most kShallowTiles tiles per CTA, which have nothing to gain
 // from a deeper ring and run faster with the smaller allocation, and 160 KB
-// for longer loops, which prefetch one tile deeper.
+// for longer loops, which prefetch one tile deeper and split it into a K ring
+// (3/5 of it) and a V ring.
 constexpr int kRingShallowKB = 128;
 constexpr int kRingDeepKB = 160;
 constexpr int kShallowTiles = 4;
@@ -74,22 +79,32 @@ struct Layout {
   static constexpr int Q_BLOCK = kBM * 128;         // one 64-column block of Q: 128 rows x 128 B
   static constexpr int Q_BYTES = KB * Q_BLOCK;
   static constexpr int TILE = static_cast<int>(tile_bytes(D));   // one K or V tile: [KB][64][128 B]
-  static constexpr int NS_FIT = (RING_KB * 1024) / TILE;
-  static constexpr int NS = NS_FIT > 16 ? 16 : NS_FIT;   // ring slots (5 at D = 256)
+  static constexpr bool SPLIT = RING_KB > kRingShallowKB;   // separate K and V rings
+  static constexpr int RING = RING_KB * 1024;
+  static constexpr int NS_FIT = RING / TILE;
+  static constexpr int NS = NS_FIT > 16 ? 16 : NS_FIT;     // single ring: slots (4 at D = 256)
+  static constexpr int NK_FIT = (RING * 3 / 5) / TILE;
+  static constexpr int NK = NK_FIT > 16 ? 16 : NK_FIT;     // split: K slots (3 at D = 256)
+  static constexpr int V_BYTES = RING - NK * TILE;          // split: V ring, cut at run time into
+                                                            // slots of one CTA's V columns
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = OFF_Q + Q_BYTES;
-  static constexpr int OFF_BAR = OFF_RING + NS * TILE;
-  static constexpr int OFF_MISC = OFF_BAR + 64 * 8;
+  static constexpr int OFF_RING = OFF_Q + Q_BYTES;          // the single ring, or the K ring
+  static constexpr int OFF_VRING = OFF_RING + NK * TILE;    // split: the V ring
+  static constexpr int OFF_BAR = OFF_RING + (SPLIT ? RING : NS * TILE);
+  static constexpr int OFF_MISC = OFF_BAR + 80 * 8;
   static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;        // slack for 1024-byte alignment
   static constexpr int TMEM_COLS = (D + 3 * kBN) <= 256 ? 256 : 512;   // O, S x 2, P x 2
   static_assert(ALLOC <= 232448, "shared memory budget");
-  static_assert(NS >= 4 && NS <= 16, "ring depth");
+  static_assert(SPLIT ? (NK >= 2 && V_BYTES >= 2 * TILE) : (NS >= 4), "ring depth");
 };
 
-// Barrier indices: Q, ring full[NS], ring empty[NS], S full[2], P full[2],
-// PV done[2], drain.
-enum : int { B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_SF = 33, B_PF = 35, B_PV = 37, B_DRAIN = 39 };
+// Barrier indices: Q, ring full / empty [16] (the single ring, or the K ring),
+// V ring full / empty [16], S full[2], P full[2], PV done[2], drain.
+enum : int {
+  B_Q = 0, B_FULL = 1, B_EMPTY = 17, B_VFULL = 33, B_VEMPTY = 49, B_SF = 65, B_PF = 67, B_PV = 69,
+  B_DRAIN = 71
+};
 
 // One group of query rows: the action suffix, or a dense batch of language
 // streams.  Its M-tiles occupy workspace rows [row_base, row_base + m_tiles*128).
@@ -201,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + Lay::OFF_Q;
   const uint32_t sRing = base + Lay::OFF_RING;
+  const uint32_t sVring = base + Lay::OFF_VRING;
   const uint32_t sBar = base + Lay::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lay::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lay::OFF_MISC + 4);
@@ -218,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_Q), 1);
-    for (int i = 0; i < Lay::NS; ++i) {
+    for (int i = 0; i < 16; ++i) {
       mbar_init(BAR(B_FULL + i), 1);
       mbar_init(BAR(B_EMPTY + i), 1);
+      mbar_init(BAR(B_VFULL + i), 1);
+      mbar_init(BAR(B_VEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_SF + i), 1);
@@ -291,65 +309,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t tP = tS + 2 * kBN;                       // two P buffers of 32 columns (bf16 pairs)
 
   const int qtok = kBM / p.G;   // query tokens per tile
-  const int ns = Lay::NS;   // ring slots
+  const int ns = Lay::NS;                                    // single ring: slots
+  const uint32_t vtile = static_cast<uint32_t>(DV) * 128;      // split: one V slot
+  const int nv_fit = Lay::SPLIT ? static_cast<int>(Lay::V_BYTES / vtile) : 2;
+  const int nv = nv_fit > 16 ? 16 : nv_fit;                  // split: V slots
   // The softmax thread's final row state, for the cluster merge.
   float fin_m = -INFINITY, fin_l = 0.f;
   bool fin_have = false;
 
+  // One K (kv = 0) or V (kv = 1) tile into shared memory at dst, counted on bar.
+  auto issue_tile = [&](const TileInfo& ti, int kv, uint32_t dst, uint32_t bar) {
+    // K: all D/64 column blocks; V: only the blocks of this CTA's columns.
+    const int kb0 = kv ? dcol / 64 : 0;
+    const int nkb = kv ? DV / 64 : Lay::KB;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nkb * 8192));
+    const uint8_t* tiles = ti.region < 2 ? (kv ? p.v_tiles[ti.region] : p.k_tiles[ti.region]) : nullptr;
+    if (tiles) {
+      bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE +
+                         kb0 * 8192,
+                static_cast<uint32_t>(nkb * 8192), bar);
+    } else {
+      const int lay = ti.region == 2 ? 0 : p.layer;
+      const CUtensorMap* tm = ti.region == 2 ? (kv ? &sg.tm_vp : &sg.tm_kp)
+                                             : (kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region]);
+      for (int kb = 0; kb < nkb; ++kb)
+        tma_load_4d(dst + kb * 8192, tm, (kb0 + kb) * 64, g, ti.phys0, lay, bar);
+    }
+  };
+
   if (n > 0 && warp == 0) {
     // ------------------------------------------------------------ producer
-    // Ring order: K_0, V_0, K_1, V_1, ...; item i uses slot i % ns.
-    if (lane == 0) {
+    // Lane 0 issues Q first.  Single ring: lane 0 then issues K_0, V_0, K_1,
+    // V_1, ...; item i uses slot i % ns.  Split rings: lane 0 issues K_j into
+    // K slot j % NK and lane 1 V_j into V slot j % nv, independently.
+    const int kv_lane = Lay::SPLIT ? lane : 0;   // split: 0 = K, 1 = V
+    if (lane == 0 || (Lay::SPLIT && lane == 1)) {
+      const int rs = Lay::SPLIT ? (kv_lane ? nv : Lay::NK) : ns;
+      const int bfull = kv_lane ? B_VFULL : B_FULL, bempty = kv_lane ? B_VEMPTY : B_EMPTY;
+      const uint32_t rbase = kv_lane ? sVring : sRing;
+      const uint32_t rstride = kv_lane ? vtile : static_cast<uint32_t>(Lay::TILE);
+      const int per_tile = Lay::SPLIT ? 1 : 2;   // items per key tile in this lane's ring
+      if (lane == 0) {
+        mbar_arrive_expect_tx(BAR(B_Q), Lay::Q_BYTES);
+        for (int kb = 0; kb < Lay::KB; ++kb)
+          tma_load_4d(sQ + kb * Lay::Q_BLOCK, &sg.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
+      }
       int issued = 0;
-      int slot = 0, rnd = 0;   // issued % ns and issued / ns, kept without dividing
-      mbar_arrive_expect_tx(BAR(B_Q), Lay::Q_BYTES);
-      for (int kb = 0; kb < Lay::KB; ++kb)
-        tma_load_4d(sQ + kb * Lay::Q_BLOCK, &sg.tm_q, kb * 64, 0, g, mt * qtok, BAR(B_Q));
-      for (int j = 0; j < n && issued >= 0; ++j) {
+      int slot = 0, rnd = 0;   // issued % rs and issued / rs, kept without dividing
+      bool stop = false;
+      for (int j = 0; j < n && !stop; ++j) {
         const TileInfo ti = tile_at(t0 + j, nt_pin, nt_win, p.P, win_len, sg.n_priv, hole0, hole_n);
-        const int lay = ti.region == 2 ? 0 : p.layer;
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = issued;
-          if (rnd > 0 && !mbar_wait(BAR(B_EMPTY + slot), (rnd - 1) & 1, abort_flag)) {
-            issued = -issued - 1;   // stop; remember how many were issued
+        for (int k = 0; k < per_tile; ++k) {
+          if (rnd > 0 && !mbar_wait(BAR(bempty + slot), (rnd - 1) & 1, abort_flag)) {
+            stop = true;
             break;
           }
-          const uint32_t dst = sRing + slot * Lay::TILE;
-          // K: all D/64 column blocks; V: only the blocks of this CTA's columns.
-          const int kb0 = kv ? dcol / 64 : 0;
-          const int nkb = kv ? DV / 64 : Lay::KB;
-          mbar_arrive_expect_tx(BAR(B_FULL + slot), static_cast<uint32_t>(nkb * 8192));
-          const uint8_t* tiles = ti.region < 2 ? (kv ? p.v_tiles[ti.region] : p.k_tiles[ti.region]) : nullptr;
-          if (tiles) {
-            bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE +
-                               kb0 * 8192,
-                      static_cast<uint32_t>(nkb * 8192), BAR(B_FULL + slot));
-          } else {
-            const CUtensorMap* tm = ti.region == 2 ? (kv ? &sg.tm_vp : &sg.tm_kp)
-                                                   : (kv ? &p.tm_v[ti.region] : &p.tm_k[ti.region]);
-            for (int kb = 0; kb < nkb; ++kb)
-              tma_load_4d(dst + kb * 8192, tm, (kb0 + kb) * 64, g, ti.phys0, lay, BAR(B_FULL + slot));
-          }
-          issued = it + 1;
-          if (++slot == ns) {
+          issue_tile(ti, Lay::SPLIT ? kv_lane : k, rbase + slot * rstride, BAR(bfull + slot));
+          ++issued;
+          if (++slot == rs) {
             slot = 0;
             ++rnd;
           }
         }
       }
-      if (issued < 0) issued = -issued - 1;
       // Every copy issued must land before the CTA exits, even after an abort.
       volatile int no_abort = 0;
-      mbar_wait(BAR(B_Q), 0, &no_abort);
-      for (int it = issued - ns < 0 ? 0 : issued - ns; it < issued; ++it)
-        mbar_wait(BAR(B_FULL + it % ns), (it / ns) & 1, &no_abort);
+      if (lane == 0) mbar_wait(BAR(B_Q), 0, &no_abort);
+      for (int it = issued - rs < 0 ? 0 : issued - rs; it < issued; ++it)
+        mbar_wait(BAR(bfull + it % rs), (it / rs) & 1, &no_abort);
     }
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
       bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
-      int slot = 0, rnd = 0;   // of item 2j
+      // K_j: item 2j of the single ring, or item j of the K ring
+      constexpr int kStep = Lay::SPLIT ? 1 : 2;
+      constexpr int kSlots = Lay::SPLIT ? Lay::NK : Lay::NS;
+      int slot = 0, rnd = 0;
       for (int j = 0; ok && j < n; ++j) {
         const int st = j & 1;
         // S buffer st last held S_{j-2}; the softmax is done with it once it
@@ -369,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
         umma_commit(BAR(B_EMPTY + slot));
         umma_commit(BAR(B_SF + st));
-        if ((slot += 2) >= ns) {
-          slot -= ns;
+        if ((slot += kStep) >= kSlots) {
+          slot -= kSlots;
           ++rnd;
         }
       }
@@ -383,13 +420,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // ------------------------------------------------------------ P V issuer
     if (lane == 0) {
       const uint32_t kIdescO = idesc_bf16_f32(kBM, DV, false, true);
-      int slot = 1, rnd = 0;   // of item 2j + 1 (ns >= 2)
+      // V_j: item 2j + 1 of the single ring, or item j of the V ring
+      const int vStep = Lay::SPLIT ? 1 : 2;
+      const int vSlots = Lay::SPLIT ? nv : ns;
+      const int bvfull = Lay::SPLIT ? B_VFULL : B_FULL, bvempty = Lay::SPLIT ? B_VEMPTY : B_EMPTY;
+      const uint32_t vbase = Lay::SPLIT ? sVring : sRing;
+      const uint32_t vstride = Lay::SPLIT ? vtile : static_cast<uint32_t>(Lay::TILE);
+      int slot = Lay::SPLIT ? 0 : 1, rnd = 0;
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         if (!mbar_wait(BAR(B_PF + st), (j >> 1) & 1, abort_flag)) break;
-        if (!mbar_wait(BAR(B_FULL + slot), rnd & 1, abort_flag)) break;
+        if (!mbar_wait(BAR(bvfull + slot), rnd & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t vt = sRing + slot * Lay::TILE;
+        const uint32_t vt = vbase + slot * vstride;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // A = P (K-major, 128 x 64 keys); B = V tile read MN-major: D runs
@@ -398,10 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           const uint64_t b = sdesc_sw128(vt + kk * 16 * 128, 8192, 1024);
           umma_bf16_ts(tO, tP + st * (kBN / 2) + kk * 8, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(BAR(B_EMPTY + slot));
+        umma_commit(BAR(bvempty + slot));
         umma_commit(BAR(B_PV + st));
-        if ((slot += 2) >= ns) {
-          slot -= ns;
+        if ((slot += vStep) >= vSlots) {
+          slot -= vSlots;
           ++rnd;
         }
       }
