@@ -278,6 +278,30 @@ def test_long_suffix_many_query_tiles(rx, splits):
     cache.close()
 
 
+@pytest.mark.parametrize("D,dparts", [(64, 1), (128, 1), (128, 2), (256, 1), (256, 2), (256, 4)])
+def test_long_key_loop_separate_k_and_v_rings(rx, D, dparts):
+    """Key loops longer than four tiles run the deeper build, whose K and V
+    tiles go through separate rings: K slots by the score tile, V slots by
+    the P V tile, the V ring cut into 2 to 8 slots by the column share.  One
+    split walks 14 key tiles (wrapping each ring several times) against the
+    oracle."""
+    wl = W.Workload("long-loop-d%d" % D, L=1, Hq=4, Hkv=1, D=D, P=64, N=3, F=256, S=40, steps=1, ticks=1,
+                    d_model=128, emb_dim=16, state_dim=16, hidden=64)
+    seed = 23 + D + dparts
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(1)
+    cache.set_attn_dparts(dparts)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    got = host64(_attend(cache, wl, seed, wl.N, 0, 0))
+    check_attention(got, _oracle_attend(ost, wl, seed, wl.N, 0, 0))
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
 def test_2048_token_suffix_one_split_per_tile(rx):
     """A 2048-token suffix over an 8-frame window (16384 query rows, 128 query
     tiles, 4160 keys): the automatic partition gives every query tile one CTA
