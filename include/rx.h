@@ -274,6 +274,16 @@ rx_status rx_export_window(rx_cache_t cache, int layer, void* k_out,
  * is cleared by this call. */
 rx_status rx_check_device_error(rx_cache_t cache, int* code, void* stream);
 
+/* Test aid for the bounded waits: the next attention launch of this cache
+ * has its first CTA expect `bytes` more on its first K tile's barrier than
+ * the copy delivers.  That barrier never completes, the CTA's waits give up
+ * after their time limit (2 s), the kernel unwinds (waiting, bounded, for its
+ * own copies and tensor-core work) and sets bit 1 of the error word, which
+ * rx_check_device_error reports; that launch's output is undefined.  Later
+ * launches are unaffected.  bytes: a multiple of 16 in [0, 2^20]; 0 cancels.
+ * Errors: RX_ERR_ARG. */
+rx_status rx_debug_inject_timeout(rx_cache_t cache, int bytes);
+
 /* Number of split-KV partitions for attention launches of this cache
  * (0 = chosen from the SM count, the default).  A tuning knob: results are
  * the same for every value up to rounding order. */

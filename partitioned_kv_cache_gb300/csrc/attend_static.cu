@@ -157,6 +157,7 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
     a.max_splits = static_cast<int>(use_splits);
     a.forced_splits = 0;
     a.forced_dparts = 0;
+    a.inject_tx = 0;
     a.num_sms = sms;
     rx::AttnSegment seg{q, k_dyn, v_dyn, out, S, n_dyn, nullptr, 1, 0, 0};
     e = rx::launch_partitioned_attention(a, &seg, 1, s, nullptr);

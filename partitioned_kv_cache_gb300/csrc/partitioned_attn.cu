@@ -141,6 +141,7 @@ struct AttnParams {
   int n_splits;
   int dparts;            // output columns split over dparts CTAs (each computes S in full)
   int fused;             // 1: the splits of an M-tile form a cluster and merge on chip
+  int inject_tx;         // test aid: extra bytes CTA 0 expects on its first K tile
   float scale_log2;      // log2(e) / sqrt(D)
 };
 
@@ -317,12 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   float fin_m = -INFINITY, fin_l = 0.f;
   bool fin_have = false;
 
-  // One K (kv = 0) or V (kv = 1) tile into shared memory at dst, counted on bar.
-  auto issue_tile = [&](const TileInfo& ti, int kv, uint32_t dst, uint32_t bar) {
+  // One K (kv = 0) or V (kv = 1) tile into shared memory at dst, counted on
+  // bar, which expects `extra` bytes more than the tile (a test aid: they
+  // never arrive, so the waits on bar run out).
+  auto issue_tile = [&](const TileInfo& ti, int kv, uint32_t dst, uint32_t bar, uint32_t extra) {
     // K: all D/64 column blocks; V: only the blocks of this CTA's columns.
     const int kb0 = kv ? dcol / 64 : 0;
     const int nkb = kv ? DV / 64 : Lay::KB;
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nkb * 8192));
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nkb * 8192) + extra);
     const uint8_t* tiles = ti.region < 2 ? (kv ? p.v_tiles[ti.region] : p.k_tiles[ti.region]) : nullptr;
     if (tiles) {
       bulk_load(dst, tiles + g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE +
@@ -364,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             stop = true;
             break;
           }
-          issue_tile(ti, Lay::SPLIT ? kv_lane : k, rbase + slot * rstride, BAR(bfull + slot));
+          const bool first_k = issued == 0 && lane == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+          issue_tile(ti, Lay::SPLIT ? kv_lane : k, rbase + slot * rstride, BAR(bfull + slot),
+                     first_k ? static_cast<uint32_t>(p.inject_tx) : 0u);
           ++issued;
           if (++slot == rs) {
             slot = 0;
@@ -990,6 +995,7 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   const bool deep = (t_max + splits - 1) / splits > kShallowTiles;
   prm.n_splits = splits;
   prm.dparts = dparts;
+  prm.inject_tx = a.inject_tx;
   prm.fused = fused ? 1 : 0;
   if (used_splits) *used_splits = splits;
   switch (a.D) {

@@ -131,6 +131,7 @@ struct rx_cache {
   long long host_pushes = 0;
   int forced_splits = 0;
   int forced_dparts = 0;
+  int inject_tx = 0;   // rx_debug_inject_timeout: applies to the next attention launch
 };
 
 #define RX_GUARD_BEGIN try {
@@ -376,6 +377,8 @@ static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   a.forced_splits = h->forced_splits;
   a.forced_dparts = h->forced_dparts;
   a.num_sms = h->num_sms;
+  a.inject_tx = h->inject_tx;
+  h->inject_tx = 0;
   return a;
 }
 
@@ -676,6 +679,16 @@ rx_status rx_set_attn_splits(rx_cache_t h, int splits) {
   if (splits < 0 || splits > h->max_splits)
     return fail(RX_ERR_ARG, "rx_set_attn_splits: %d not in [0, %d]", splits, h->max_splits);
   h->forced_splits = splits;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_debug_inject_timeout(rx_cache_t h, int bytes) {
+  RX_GUARD_BEGIN
+  if (!h) return fail(RX_ERR_ARG, "rx_debug_inject_timeout: null cache");
+  if (bytes < 0 || bytes > (1 << 20) || (bytes & 15))
+    return fail(RX_ERR_ARG, "rx_debug_inject_timeout: %d not a multiple of 16 in [0, 2^20]", bytes);
+  h->inject_tx = bytes;
   return RX_OK;
   RX_GUARD_END
 }

@@ -137,6 +137,7 @@ struct AttnLaunch {
   int forced_splits;  // 0 = automatic
   int forced_dparts;  // output-column split: 0 = automatic, else 1, 2 or 4
   int num_sms;
+  int inject_tx;      // test aid: extra bytes CTA 0 expects on its first K tile (0 = none)
 };
 
 // One group of query rows attending over [pinned; window; private keys].

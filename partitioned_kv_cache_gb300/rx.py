@@ -31,7 +31,7 @@ EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_fram
            "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
            "rx_attend_regions_static", "rx_attend_suffix_block_causal", "rx_tail_append",
            "rx_snapshot_bytes", "rx_snapshot", "rx_restore", "rx_push_frame_async",
-           "rx_set_attn_dparts")
+           "rx_set_attn_dparts", "rx_debug_inject_timeout")
 
 
 class RxConfig(ctypes.Structure):
@@ -63,6 +63,7 @@ _sigs = {
     "rx_check_device_error": (_i, [_vp, ctypes.POINTER(_i), _vp]),
     "rx_set_attn_splits": (_i, [_vp, _i]),
     "rx_set_attn_dparts": (_i, [_vp, _i]),
+    "rx_debug_inject_timeout": (_i, [_vp, _i]),
     "rx_launch_count": (ctypes.c_longlong, []),
     "rx_status_str": (ctypes.c_char_p, [_i]),
     "rx_last_error": (ctypes.c_char_p, []),
@@ -262,6 +263,11 @@ class Cache:
 
     def set_attn_dparts(self, dparts: int) -> None:
         _check(_lib.rx_set_attn_dparts(self._h, dparts), "rx_set_attn_dparts")
+
+    def debug_inject_timeout(self, nbytes: int) -> None:
+        """Test aid: the next attention launch's first CTA waits for nbytes
+        that never arrive, so its bounded waits run out (see rx.h)."""
+        _check(_lib.rx_debug_inject_timeout(self._h, nbytes), "rx_debug_inject_timeout")
 
 
 def ada_gamma(t: torch.Tensor, state: torch.Tensor, W1: torch.Tensor, b1: torch.Tensor,

@@ -91,3 +91,4 @@ def test_cache_calls_reject_null_handle(lib):
     assert L.rx_attend_batch(None, 0, None, None, None, 0, None, None, None) == -1
     assert L.rx_set_attn_splits(None, 0) == -1
     assert L.rx_set_attn_dparts(None, 0) == -1
+    assert L.rx_debug_inject_timeout(None, 16) == -1

@@ -373,3 +373,32 @@ def test_running_maximum_rescale(rx, splits):
     assert np.all(err <= bound), "worst err / bound %.2f" % float(np.max(err / bound))
     assert cache.check_device_error() == 0
     cache.close()
+
+
+@pytest.mark.parametrize("splits", [1, 0])
+def test_bounded_wait_gives_up_and_reports(rx, splits):
+    """A barrier that never completes (the first K tile's barrier of CTA 0
+    expects 16 bytes that never arrive): the kernel's waits give up after
+    their time limit instead of hanging, the cache's error word reports it
+    (bit 1), and the next call on the same cache matches the oracle."""
+    import time
+    wl = W.WORKLOADS["c2"]
+    seed = 31
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(splits)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    with pytest.raises(rx.RxError):
+        cache.debug_inject_timeout(15)
+    cache.debug_inject_timeout(16)
+    t0 = time.time()
+    _attend(cache, wl, seed, wl.N - 1, 0, 0)
+    assert cache.check_device_error() & 1
+    assert time.time() - t0 < 30
+    got = host64(_attend(cache, wl, seed, wl.N - 1, 0, 0))
+    check_attention(got, _oracle_attend(ost, wl, seed, wl.N - 1, 0, 0))
+    assert cache.check_device_error() == 0
+    cache.close()
