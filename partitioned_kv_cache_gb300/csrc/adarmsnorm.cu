@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -39,6 +40,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// SM count of device `dev`, queried once per device.
+cudaError_t device_sm_count(int dev, int* out) {
+  static std::atomic<int> cache[64];
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && (*out = cache[dev].load(std::memory_order_relaxed)) > 0) return cudaSuccess;
+  const cudaError_t e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && cached) cache[dev].store(*out, std::memory_order_relaxed);
+  return e;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -51,13 +62,22 @@ template <int MAXV>
 __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict__ x,
                                                          const float* __restrict__ gamma,
                                                          int rows, int d, float eps,
-                                                         uint4* __restrict__ y) {
-  grid_dependency_wait();
-  grid_launch_dependents();
+                                                         uint4* __restrict__ y, int prefetch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;
-  if (row >= rows) return;
   const int nv = d >> 3;
+  // A launch that fits on the GPU at once fetches its rows and gamma towards
+  // L2 while the previous kernel finishes (a hint: safe before the dependency
+  // wait), so the loads below do not pay the DRAM latency inside the launch
+  // chain.  Larger launches skip it: their later CTAs start long after the
+  // wait, and the extra requests only cost bandwidth.
+  if (prefetch) {
+    if (lane == 0 && row < rows) bulk_prefetch_l2(x + row * nv, static_cast<uint32_t>(d) * 2u);
+    if (threadIdx.x == 32 * 7 + 1) bulk_prefetch_l2(gamma, static_cast<uint32_t>(d) * 4u);
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (row >= rows) return;
   const uint4* xr = x + row * nv;
   uint4* yr = y + row * nv;
   const float inv_d = 1.0f / static_cast<float>(d);
@@ -262,11 +282,7 @@ __global__ void __launch_bounds__(kGThreads, 1) ada_gamma_kernel(const __grid_co
       mbar_arrive_expect_tx(FULL(issued), kGBlock);
       tma_load_4d(sRing + issued * kGBlock, &a.tm_w2, issued * 64, tile * kGM, set, 0, FULL(issued));
     }
-    for (int b = kGSlots; b < nkb; ++b)
-      asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                       reinterpret_cast<uint64_t>(&a.tm_w2)),
-                   "r"(b * 64), "r"(tile * kGM), "r"(set), "r"(0)
-                   : "memory");
+    for (int b = kGSlots; b < nkb; ++b) tma_prefetch_l2_4d(&a.tm_w2, b * 64, tile * kGM, set, 0);
   }
 
   const int half = a.emb_dim / 2;
@@ -423,16 +439,20 @@ cudaError_t launch_adarmsnorm(const __nv_bfloat16* x, const float* gamma, int ro
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint4* yv = reinterpret_cast<uint4*>(y);
   cudaError_t e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = device_sm_count(dev, &sms)) != cudaSuccess) return e;
+  const int pf = blocks <= static_cast<unsigned int>(sms) ? 1 : 0;
   if (d <= 256)
-    e = launch_k(adarmsnorm_kernel<1>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<1>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv, pf);
   else if (d <= 512)
-    e = launch_k(adarmsnorm_kernel<2>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<2>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv, pf);
   else if (d <= 1024)
-    e = launch_k(adarmsnorm_kernel<4>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<4>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv, pf);
   else if (d <= 2048)
-    e = launch_k(adarmsnorm_kernel<8>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<8>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv, pf);
   else
-    e = launch_k(adarmsnorm_kernel<0>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv);
+    e = launch_k(adarmsnorm_kernel<0>, dim3(blocks), dim3(256), 0, s, xv, gamma, rows, d, eps, yv, pf);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
