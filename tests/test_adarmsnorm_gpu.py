@@ -39,7 +39,10 @@ def test_gamma_matches_oracle(rx, name, n_sets):
             np.testing.assert_allclose(gamma[i, k], ref, rtol=0, atol=2e-5)
 
 
-@pytest.mark.parametrize("rows,d", [(51, 1024), (8, 128), (3, 4096), (5, 8), (1, 2048), (300, 1000)])
+# Up to one CTA (8 rows) per SM the kernel prefetches its rows into L2 before
+# the dependency wait; the last two sizes are larger than that on GB300.
+@pytest.mark.parametrize("rows,d", [(51, 1024), (8, 128), (3, 4096), (5, 8), (1, 2048), (300, 1000),
+                                    (2000, 1024), (1300, 40)])
 def test_norm_matches_oracle_across_magnitudes(rx, rows, d):
     import torch
     x = W.magnitude_sweep(rows, d, seed=rows * d)
