@@ -180,10 +180,15 @@ __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // swizzle atoms are 1 KB
   const uint32_t bar = base + static_cast<uint32_t>(tile_bytes(a.D));
+  const int l = blockIdx.y / a.Hkv, g = blockIdx.y % a.Hkv, kv = blockIdx.z;
+  // The source tile is fetched towards L2 while the previous kernel finishes
+  // (a hint: safe before the dependency wait), so the boxes below come from
+  // L2 rather than DRAM.
+  if (threadIdx.x == 0)
+    for (int kb = 0; kb < a.D / 64; ++kb) tma_prefetch_l2_4d(&a.tm[kv], kb * 64, g, blockIdx.x * kTileTok, l);
   grid_dependency_wait();
   grid_launch_dependents();
   if (threadIdx.x != 0) return;
-  const int l = blockIdx.y / a.Hkv, g = blockIdx.y % a.Hkv, kv = blockIdx.z;
   const uint32_t bytes = static_cast<uint32_t>(tile_bytes(a.D));
   // The source boxes do not depend on the ring state: issue them first and
   // read the state while they are in flight.
