@@ -321,7 +321,7 @@ const char* rx_last_error(void);
  * partials and a small state block) lives in one fixed device array of
  * RX_STATIC_SCRATCH_BYTES that every GPU loading this library holds until
  * the process exits.  Limit: Hkv * ceil(S*Hq/Hkv / 128) * 128 *
- * (4*D + 8) bytes must fit in that array (about 8000 query rows at D = 256);
+ * (2*D + 32) bytes must fit in that array (about 15 000 query rows at D = 256);
  * larger calls return RX_ERR_CAPACITY.  The first call on each device looks
  * up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Every call shares

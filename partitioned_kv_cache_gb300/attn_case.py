@@ -7,7 +7,8 @@ one launch of the attention kernel can be captured in isolation:
 
     python -m partitioned_kv_cache_gb300.attn_case --workload c4 --layers 2 --calls 6
 
-(--suffix replaces the workload's suffix length, e.g. 1024 query tokens.)
+(--suffix replaces the workload's suffix length, e.g. 1024 query tokens;
+--splits and --dparts force the partition, 0 = automatic.)
 
 --op gamma issues the gamma-MLP launch of one tick of the workload (all 2L
 norm sites x K steps) a few times, each on its own weight set:
@@ -42,6 +43,8 @@ def main(argv=None) -> None:
     ap.add_argument("--frame-mult", type=int, default=1)
     ap.add_argument("--rows", type=int, default=0)
     ap.add_argument("--suffix", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--dparts", type=int, default=0)
     a = ap.parse_args(argv)
     wl = W.WORKLOADS[a.workload]
     L = max(1, min(a.layers, wl.L))
@@ -91,6 +94,8 @@ def main(argv=None) -> None:
 
     S = a.suffix if a.suffix > 0 else wl.S
     cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, S)
+    cache.set_attn_splits(a.splits)
+    cache.set_attn_dparts(a.dparts)
     cache.pin_prefix(r(L, wl.P, wl.Hkv, wl.D), r(L, wl.P, wl.Hkv, wl.D))
     for _ in range(wl.N):
         cache.push_frame(r(L, wl.F, wl.Hkv, wl.D), r(L, wl.F, wl.Hkv, wl.D))

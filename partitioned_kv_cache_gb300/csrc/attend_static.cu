@@ -81,7 +81,8 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
       return reject(RX_ERR_ARG, "pointers must be 16-byte aligned");
 
     const size_t rows_pad = (static_cast<size_t>(S) * G + rx::kBM - 1) / rx::kBM * rx::kBM;
-    const size_t per_split = static_cast<size_t>(Hkv) * rows_pad * (static_cast<size_t>(D) * 4 + 8);
+    // Split partials: per row and split, D bf16 values and up to 4 (m, l) pairs.
+    const size_t per_split = static_cast<size_t>(Hkv) * rows_pad * (static_cast<size_t>(D) * 2 + 32);
     const size_t fit = (kScratchBytes - kStateBytes) / per_split;
     if (fit < 1) return reject(RX_ERR_CAPACITY, "Hkv * S * Hq/Hkv query rows exceed the 8 MiB static scratch");
 
@@ -97,18 +98,10 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
     e = scratch_address(dev, &base);
     if (e != cudaSuccess) return reject(RX_ERR_CUDA, cudaGetErrorString(e));
 
-    // Scratch layout: [DevState | (m, l) partials | O partials].
+    // Scratch layout: [DevState | split partials].
     char* sb = static_cast<char*>(base);
     rx::DevState* st = reinterpret_cast<rx::DevState*>(sb);
-    const size_t splits_cap = fit < 1024 ? fit : 1024;
-    float2* part_ml = reinterpret_cast<float2*>(sb + kStateBytes);
-    const size_t ml_bytes = (static_cast<size_t>(Hkv) * splits_cap * rows_pad * sizeof(float2) + 255) / 256 * 256;
-    float* part_o = reinterpret_cast<float*>(sb + kStateBytes + ml_bytes);
-    size_t use_splits = splits_cap;
-    while (use_splits > 1 && kStateBytes + ml_bytes +
-                                 static_cast<size_t>(Hkv) * use_splits * rows_pad * D * sizeof(float) >
-                             kScratchBytes)
-      --use_splits;
+    const size_t use_splits = fit < 64 ? fit : 64;
 
     // The kernel reads the window length as valid * F from the state block;
     // here the window is one run of W tokens (F = 1).  Every call rewrites the
@@ -152,8 +145,7 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
     a.Hkv = Hkv;
     a.st = st;
     a.err = &st->err;
-    a.part_o = part_o;
-    a.part_ml = part_ml;
+    a.xchg = sb + kStateBytes;
     a.max_splits = static_cast<int>(use_splits);
     a.forced_splits = 0;
     a.forced_dparts = 0;

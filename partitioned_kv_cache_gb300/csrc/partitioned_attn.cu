@@ -29,14 +29,14 @@
 //     shared memory.  O is rescaled in TMEM only when the running maximum
 //     grows by more than 2^8 (otherwise the stale maximum is kept: exact after
 //     the final division by the row sum).
-//   * The key sequence is split across CTAs (gridDim.y).  When the splits of an
-//     M-tile form one thread-block cluster (up to kMaxClusterSplits), every
-//     split writes its normalised partial O / l (bf16) and fp32 (m, l) to an
-//     exchange area in L2, the cluster passes one barrier, and each CTA then
+//   * The key sequence is split across CTAs (gridDim.y).  Every split writes
+//     its normalised partial O / l (bf16) and fp32 (m, l) to an exchange area
+//     in L2.  When the splits of an M-tile form one thread-block cluster (up
+//     to kMaxClusterSplits), the cluster passes one barrier and each CTA then
 //     combines a block of rows from all C partials and writes the bf16
-//     output: no second kernel runs.  Beyond that size each split writes an
-//     fp32 partial to global memory and a merge kernel combines them.  With a
-//     single split the CTA writes the bf16 output directly.
+//     output: no second kernel runs.  Beyond that size a combine kernel reads
+//     the same exchange area.  With a single split the CTA writes the bf16
+//     output directly.
 //   * The output columns of a (tile, split) may be shared by dparts CTAs: each
 //     computes S in full but loads only its D/dparts columns of V, so its key
 //     loop moves fewer bytes and its partial is dparts times smaller.
@@ -130,8 +130,7 @@ struct AttnParams {
   const uint8_t* k_tiles[2];   // pre-tiled pin / window of (layer, head 0); null = tensor map
   const uint8_t* v_tiles[2];
   long long head_stride[2];    // bytes between heads of a tiled region
-  float* part_o;         // [Hkv][splits][D][rows_pad] (column-major per split)
-  float2* part_ml;       // [Hkv][splits][rows_pad]
+  void* xchg;            // split partials: see the split merge in attn_kernel
   const DevState* st;
   int* err;
   int layer;
@@ -206,6 +205,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   const bool ok = mbar_wait(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Exchange area of the split partials, per (tile, head, column share) unit
+// u = blockIdx.z * gridDim.x + blockIdx.x: O [splits][D/dparts/8 pieces][128
+// rows] of 16 bytes for every unit, then (m, l) [splits][128] for every unit.
+__device__ __forceinline__ uint4* xchg_o(const AttnParams& p, int DV, int split) {
+  const size_t u = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
+  return reinterpret_cast<uint4*>(p.xchg) + (u * p.n_splits + split) * (DV / 8) * kBM;
+}
+__device__ __forceinline__ float2* xchg_ml(const AttnParams& p, int DV, int split) {
+  const size_t u = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
+  return reinterpret_cast<float2*>(reinterpret_cast<uint4*>(p.xchg) +
+                                   static_cast<size_t>(gridDim.x) * gridDim.z * p.n_splits * (DV / 8) * kBM) +
+         (u * p.n_splits + split) * kBM;
 }
 
 template <int D, int RING_KB>
@@ -464,8 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int Rs = mt * kBM + row;                     // row within the segment
     const bool row_valid = Rs < sg.rows;
-    const int R = sg.row_base + Rs;                    // row within the workspace
-    const size_t part_idx = (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad + R;
     // Private-key window of this row: its stream's tail (stream mask) or the
     // state block's own keys (block-causal suffix); [0, n_priv) otherwise.
     int lo = 0, hi = sg.n_priv;
@@ -576,23 +587,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         fin_l = l;
         fin_have = true;
       } else {
-        // Partial O is stored column-major per split ([D][rows_pad]): for each
-        // column the 32 lanes of a warp write 32 consecutive rows (128 B).
-        float* dst = p.part_o + (static_cast<size_t>(g) * p.n_splits + split) * p.rows_pad * D +
-                     static_cast<size_t>(dcol) * p.rows_pad + R;
+        // More splits than a cluster: this row's partial goes to the exchange
+        // area in the layout of the cluster merge below, and
+        // attn_combine_kernel combines the splits after the grid.
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* dst = xchg_o(p, DV, split) + row;
 #pragma unroll 1
         for (int c = 0; c < DV; c += 32) {
           float o[32];
           tmem_ld32(tO + c + lane_off, o);
           if (row_valid) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(c + i) * p.rows_pad] = o[i];
+            for (int q = 0; q < 4; ++q)
+              dst[static_cast<size_t>(c / 8 + q) * kBM] =
+                  make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
+                             pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                             pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                             pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
           }
         }
-        if (row_valid && dcol == 0) p.part_ml[part_idx] = make_float2(m_used, l);
+        if (row_valid) xchg_ml(p, DV, split)[row] = make_float2(m_used, l);
       }
-    } else if (n == 0 && row_valid && p.n_splits > 1 && dcol == 0) {
-      p.part_ml[part_idx] = make_float2(-INFINITY, 0.f);   // empty split: merge skips it
+    } else if (!p.fused && p.n_splits > 1 && row_valid) {
+      // A split without keys (or one that gave up): zeros and l = 0, which
+      // the combine skips.
+      uint4* dst = xchg_o(p, DV, split) + row;
+      for (int c = 0; c < DV / 8; ++c) dst[static_cast<size_t>(c) * kBM] = make_uint4(0u, 0u, 0u, 0u);
+      xchg_ml(p, DV, split)[row] = make_float2(-INFINITY, 0.f);
     }
   }
 
@@ -610,8 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int C = p.n_splits;
     const int rank = static_cast<int>(cluster_ctarank());
     const size_t cid = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
-    uint4* xo = reinterpret_cast<uint4*>(p.part_o) + cid * C * kPieces * kBM;
-    float2* xml = reinterpret_cast<float2*>(reinterpret_cast<uint4*>(p.part_o) +
+    uint4* xo = reinterpret_cast<uint4*>(p.xchg) + cid * C * kPieces * kBM;
+    float2* xml = reinterpret_cast<float2*>(reinterpret_cast<uint4*>(p.xchg) +
                                             static_cast<size_t>(gridDim.x) * gridDim.z * C * kPieces * kBM) +
                   cid * C * kBM;
     if (warp >= 2 && warp <= 5) {
@@ -706,78 +727,82 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err, kErrAttnTimeout);
 }
 
-// Combine the splits of every row: m = max m_s, l = sum 2^(m_s - m) l_s,
-// out = sum 2^(m_s - m) O_s / l.  A block covers 32 consecutive workspace rows
-// (of one segment) x 32 columns; lane r owns row r.  The four warps take every fourth split, so up
-// to eight splits' loads are in flight per lane (two per warp, unrolled), each
-// a coalesced 128-byte run of the column-major partial; the warps' sums meet
-// in shared memory.
+// Combine the splits of every row when they do not form a cluster (more than
+// kMaxClusterSplits of them), over the exchange area the attention grid
+// wrote, with the weighting of the in-kernel merge: out = sum_s w_s O_s / l_s
+// divided by sum_s w_s, where w_s = 2^(m_s - M) l_s.  One thread per (row,
+// 16-byte piece), rows fastest, so a warp's load of one split is 512
+// contiguous bytes.  Grid: (M-tiles of all segments, pieces / 2, Hkv x dparts),
+// the attention grid's x and z.  The splits are taken 16 at a time, their
+// loads in flight together, with a running maximum: a chunk that raises it
+// rescales the sums so far.
+constexpr int kCombineChunk = 16;
+
 template <int D>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o,
-                                                         const float2* __restrict__ part_ml,
-                                                         __nv_bfloat16* out0, int rows0,
-                                                         __nv_bfloat16* out1, int rows1,
-                                                         int row_base1, int rows_pad, int n_splits,
-                                                         int Hq, int G) {
-  __shared__ float red[3][32][33];
-  __shared__ float red_l[3][32];
+__global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restrict__ xchg,
+                                                           __nv_bfloat16* out0, int rows0, int m_tiles0,
+                                                           __nv_bfloat16* out1, int rows1, int n_splits,
+                                                           int dparts, int Hq, int G) {
   grid_dependency_wait();
   grid_launch_dependents();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int R = blockIdx.x * 32 + lane;               // workspace row
-  const int si = static_cast<int>(blockIdx.x) * 32 < row_base1 ? 0 : 1;   // blocks never straddle
-  const int base = si ? row_base1 : 0;
+  const int DV = D / dparts;
+  const int kPieces = DV / 8;
+  const int si = static_cast<int>(blockIdx.x) < m_tiles0 ? 0 : 1;
+  const int mt = blockIdx.x - (si ? m_tiles0 : 0);
   const int rows = si ? rows1 : rows0;
   __nv_bfloat16* out = si ? out1 : out0;
-  if (static_cast<int>(blockIdx.x) * 32 - base >= rows) return;   // padding only
-  const int Rs = R - base;
-  const int c0 = blockIdx.y * 32;
-  const int g = blockIdx.z;
-  const bool valid = Rs < rows;
-  const int Rc = valid ? R : base + rows - 1;   // keep loads on written rows
-  const size_t head = static_cast<size_t>(g) * n_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) {
-    const float2 v = part_ml[(head + s) * rows_pad + Rc];
-    if (v.y > 0.f) M = fmaxf(M, v.x);
+  const int i = threadIdx.x & (kBM - 1);
+  const int k = blockIdx.y * 2 + (threadIdx.x >> 7);
+  const int Rs = mt * kBM + i;
+  if (Rs >= rows) return;   // padding rows were never written
+  const int C = n_splits;
+  const size_t cid = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
+  const uint4* src = xchg + cid * C * kPieces * kBM + static_cast<size_t>(k) * kBM + i;
+  const float2* ml_src = reinterpret_cast<const float2*>(xchg + static_cast<size_t>(gridDim.x) * gridDim.z * C *
+                                                                    kPieces * kBM) +
+                         cid * C * kBM + i;
+  float M = -INFINITY, L = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int s0 = 0; s0 < C; s0 += kCombineChunk) {
+    uint4 pv[kCombineChunk];
+    float2 ml[kCombineChunk];
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u) {   // past the last split: re-read it, weigh 0
+      const int sc = min(s0 + u, C - 1);
+      pv[u] = __ldcg(src + static_cast<size_t>(sc) * kPieces * kBM);
+      ml[u] = __ldcg(ml_src + static_cast<size_t>(sc) * kBM);
+    }
+    float mc = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u)
+      if (s0 + u < C && ml[u].y > 0.f) mc = fmaxf(mc, ml[u].x);
+    if (mc == -INFINITY) continue;   // no split of this chunk saw a key
+    const float Mn = fmaxf(M, mc);
+    const float sc = exp2f(M - Mn);  // 0 before the first live split
+    L *= sc;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u) {
+      const float w = s0 + u < C && ml[u].y > 0.f ? exp2f(ml[u].x - Mn) * ml[u].y : 0.f;
+      L += w;
+      const uint32_t vv[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] = fmaf(w, __uint_as_float(vv[e] << 16), acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
+      }
+    }
+    M = Mn;
   }
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-  float lsum = 0.f;
-  const size_t col_off = static_cast<size_t>(c0) * rows_pad + Rc;
-#pragma unroll 2
-  for (int s = warp; s < n_splits; s += 4) {
-    const float2 v = part_ml[(head + s) * rows_pad + Rc];
-    const bool live = v.y > 0.f;
-    const float w = live ? exp2f(v.x - M) : 0.f;
-    lsum += w * v.y;
-    const float* o = part_o + (head + s) * rows_pad * D + col_off;
-    float x[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = o[static_cast<size_t>(i) * rows_pad];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] += live ? w * x[i] : 0.f;
-  }
-  if (warp > 0) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) red[warp - 1][i][lane] = acc[i];
-    red_l[warp - 1][lane] = lsum;
-  }
-  __syncthreads();
-  if (warp > 0 || !valid) return;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] += red[0][i][lane] + red[1][i][lane] + red[2][i][lane];
-  lsum += red_l[0][lane] + red_l[1][lane] + red_l[2][lane];
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;   // a row with no key at all gets zeros
+  const float inv = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
+  const int g = blockIdx.z / dparts, dcol = (blockIdx.z % dparts) * DV;
   const int tok = Rs / G, h = g * G + Rs % G;
-  uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok) * Hq + h) * D + c0);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv),
-                        pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
-                        pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
-                        pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+  *reinterpret_cast<uint4*>(out + (static_cast<size_t>(tok) * Hq + h) * D + dcol + k * 8) =
+      make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                 pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
 }
 
 template <int D, int RING_KB>
@@ -816,11 +841,10 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1 || prm.fused) return e;
-  dim3 mgrid(prm.rows_pad / 32, D / 32, Hkv);
-  e = launch_k(attn_merge_kernel<D>, mgrid, dim3(128), 0, s, static_cast<const float*>(prm.part_o),
-               static_cast<const float2*>(prm.part_ml), prm.seg[0].out, prm.seg[0].rows,
-               prm.seg[1].out, prm.seg[1].rows, prm.seg[1].row_base, prm.rows_pad, prm.n_splits,
-               prm.Hq, prm.G);
+  dim3 cgrid(m_tiles, D / prm.dparts / 16, Hkv * prm.dparts);
+  e = launch_k(attn_combine_kernel<D>, cgrid, dim3(256), 0, s, static_cast<const uint4*>(prm.xchg),
+               prm.seg[0].out, prm.seg[0].rows, prm.seg[0].m_tiles, prm.seg[1].out, prm.seg[1].rows,
+               prm.n_splits, prm.dparts, prm.Hq, prm.G);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -933,8 +957,7 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   prm.v_tiles[1] = static_cast<const uint8_t*>(a.win_v_tiles);
   prm.head_stride[0] = a.pin_head_stride;
   prm.head_stride[1] = a.win_head_stride;
-  prm.part_o = a.part_o;
-  prm.part_ml = a.part_ml;
+  prm.xchg = a.xchg;
   prm.st = a.st;
   prm.err = a.err;
   prm.layer = a.layer;

@@ -118,8 +118,7 @@ struct rx_cache {
   __nv_bfloat16* k_win = nullptr;
   __nv_bfloat16* v_win = nullptr;
   rx::DevState* dstate = nullptr;
-  float* part_o = nullptr;
-  float2* part_ml = nullptr;
+  void* xchg = nullptr;
   int max_splits = 0;
   int T_pin = 0;         // tiles of the pinned region per (layer, head), >= 1
   int T_win = 0;         // tiles of the window per (layer, head)
@@ -206,11 +205,11 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   // Workspace rows: the action suffix plus a language batch (rx_attend_batch).
   const size_t rows_pad = round_up(static_cast<size_t>(c.S_cap) * G, rx::kBM) +
                           round_up(static_cast<size_t>(c.max_req) * G, rx::kBM);
+  // Split partials: per row and split, D bf16 values and dparts (m, l) pairs.
   const size_t part_rows = static_cast<size_t>(c.Hkv) * h->max_splits * rows_pad;
-  const size_t po_b = round_up(part_rows * c.D * sizeof(float), 256);
-  const size_t pml_b = round_up(part_rows * sizeof(float2), 256);
+  const size_t xchg_b = round_up(part_rows * (2 * static_cast<size_t>(c.D) + 8 * 4), 256);
   const size_t st_b = 256;
-  h->mem_bytes = 2 * pin_b + 2 * win_b + st_b + po_b + pml_b;
+  h->mem_bytes = 2 * pin_b + 2 * win_b + st_b + xchg_b;
   e = cudaMalloc(&h->mem, h->mem_bytes);
   if (e != cudaSuccess) {
     delete h;
@@ -229,8 +228,7 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   h->k_win = reinterpret_cast<__nv_bfloat16*>(p); p += win_b;
   h->v_win = reinterpret_cast<__nv_bfloat16*>(p); p += win_b;
   h->dstate = reinterpret_cast<rx::DevState*>(p); p += st_b;
-  h->part_o = reinterpret_cast<float*>(p); p += po_b;
-  h->part_ml = reinterpret_cast<float2*>(p);
+  h->xchg = p;
   if (c.spare_slot) {
     e = cudaEventCreateWithFlags(&h->consumer_done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->push_done, cudaEventDisableTiming);
@@ -371,8 +369,7 @@ static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   a.Hkv = h->cfg.Hkv;
   a.st = h->dstate;
   a.err = &h->dstate->err;
-  a.part_o = h->part_o;
-  a.part_ml = h->part_ml;
+  a.xchg = h->xchg;
   a.max_splits = h->max_splits;
   a.forced_splits = h->forced_splits;
   a.forced_dparts = h->forced_dparts;

@@ -131,9 +131,9 @@ struct AttnLaunch {
   int slots;          // frame slots of the window: N, or N + 1 with a spare slot
   const DevState* st;
   int* err;
-  float* part_o;      // workspace: [Hkv][splits][D][tiles*128] fp32
-  float2* part_ml;    // workspace: [Hkv][splits][tiles*128]
-  int max_splits;     // capacity of the workspace in splits
+  void* xchg;         // workspace for the split partials (attention grid <-> merge):
+                      // Hkv * splits * tiles*128 * (2*D + 8*dparts) bytes
+  int max_splits;     // capacity of the workspace in splits (at dparts <= 4)
   int forced_splits;  // 0 = automatic
   int forced_dparts;  // output-column split: 0 = automatic, else 1, 2 or 4
   int num_sms;

@@ -98,8 +98,8 @@ def test_split_count_does_not_change_the_result(rx, splits):
 def test_output_column_split_does_not_change_the_result(rx, splits, dparts):
     """Every CTA of a (tile, split) computes the scores in full and the value
     product for its D/dparts columns: fused cluster merge (12, 3 splits),
-    single split (1) and the global-memory merge (20 splits) all agree with
-    the oracle."""
+    single split (1) and the combine kernel (20 splits, clamped to the 18
+    key tiles) all agree with the oracle."""
     wl = W.WORKLOADS["c2"]
     seed = 9
     cache = _make(rx, wl, seed)
@@ -191,6 +191,30 @@ def test_full_size_sampled_tokens(rx, name):
         # output magnitude (bf16 rounding is relative).
         scale = max(1.0, float(np.abs(ref).max())) if wl.outlier_frac > 0 else 1.0
         check_attention(got, ref, scale)
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
+@pytest.mark.parametrize("splits,dparts", [(17, 1), (24, 2), (33, 1), (64, 1)])
+def test_more_splits_than_a_cluster_combine_kernel(rx, splits, dparts):
+    """More splits than one cluster holds: every split writes its partial to
+    the exchange area and a separate kernel combines them, 16 splits per
+    chunk with a running maximum (33 leaves a chunk with one live split)."""
+    wl = W.WORKLOADS["c4"]
+    seed = 12
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(splits)
+    cache.set_attn_dparts(dparts)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    tokens = [0, 17, 50]
+    for layer in (0, wl.L - 1):
+        got = host64(_attend(cache, wl, seed, wl.N, 4, layer))[tokens]
+        ref = _oracle_attend(ost, wl, seed, wl.N, 4, layer, tokens=tokens)
+        check_attention(got, ref, max(1.0, float(np.abs(ref).max())))
     assert cache.check_device_error() == 0
     cache.close()
 

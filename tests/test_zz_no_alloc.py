@@ -49,7 +49,7 @@ def test_static_entry_rejects_too_many_query_rows():
     import torch
     ensure_built()
     from partitioned_kv_cache_gb300 import rx
-    S, Hq, D = 8200, 1, 256          # 8200 rows x (4*256 + 8) B > 8 MiB
+    S, Hq, D = 15500, 1, 256         # 15616 padded rows x (2*256 + 32) B > 8 MiB
     q = torch.zeros((S, Hq, D), dtype=torch.bfloat16, device="cuda")
     kd = torch.zeros((4, 1, D), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rx.RxError) as e:
