@@ -104,9 +104,9 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
-// 4-D tile fetched into L2 only: a hint with no effect on memory ordering.
-// Every write reaches L2, so a line fetched there early never hides a later
-// write, and the hint is safe before griddepcontrol.wait.
+// 4-D tile fetched into L2 only: a hint with no effect on memory ordering or
+// on what any load returns, so it is safe before griddepcontrol.wait (the
+// loads that use the data still come after the wait).
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* tm, int c0, int c1, int c2, int c3) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
                    reinterpret_cast<uint64_t>(tm)),
