@@ -221,7 +221,76 @@ __device__ __forceinline__ float2* xchg_ml(const AttnParams& p, int DV, int spli
          (u * p.n_splits + split) * kBM;
 }
 
-template <int D, int RING_KB>
+// The cluster merge's last step: rows [r0, r0 + nr) of the tile from the C
+// partial slots of the cluster.  Items are (piece k, row i) pairs, rows
+// fastest (a warp's loads of one split are consecutive 16-byte rows).  Each
+// thread takes U items per pass and loads the CM >= C partial pieces and
+// (m, l) of each together, U * CM = 16 loads in flight (splits >= C re-read
+// split C-1 and weigh 0).  The weight of split s is 2^(m_s - M) l_s / sum, as
+// the partials are O_s / l_s.
+template <int D, int U, int CM>
+__device__ __forceinline__ void cluster_combine(const uint4* xo, const float2* xml, int C, int kPieces, int r0,
+                                                int nr, int mt, const SegParams& sg, int Hq, int G, int g,
+                                                int dcol) {
+  const int items = nr * kPieces;
+  for (int base = threadIdx.x; base < items; base += kThreads * U) {
+    uint4 pv[U][CM];
+    float2 ml[U][CM];
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int item = min(base + q * kThreads, items - 1);   // past the end: re-read, not stored
+      const int i = item % nr, k = item / nr;
+      const uint4* src = xo + static_cast<size_t>(k) * kBM + r0 + i;
+#pragma unroll
+      for (int s2 = 0; s2 < CM; ++s2) {
+        const int sc = min(s2, C - 1);
+        pv[q][s2] = __ldcg(src + static_cast<size_t>(sc) * kPieces * kBM);
+        ml[q][s2] = __ldcg(xml + sc * kBM + r0 + i);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int item = base + q * kThreads;
+      const int i = item % nr, k = item / nr;
+      const int Rs = mt * kBM + r0 + i;
+      if (item >= items || Rs >= sg.rows) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int s2 = 0; s2 < CM; ++s2)
+        if (s2 < C && ml[q][s2].y > 0.f) M = fmaxf(M, ml[q][s2].x);
+      float w[CM];
+      float L = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < CM; ++s2) {
+        w[s2] = s2 < C && ml[q][s2].y > 0.f ? exp2f(ml[q][s2].x - M) * ml[q][s2].y : 0.f;
+        L += w[s2];
+      }
+      const float invL = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < CM; ++s2) {
+        const float ws = w[s2] * invL;
+        const uint32_t vv[4] = {pv[q][s2].x, pv[q][s2].y, pv[q][s2].z, pv[q][s2].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] = fmaf(ws, __uint_as_float(vv[e] << 16), acc[2 * e]);
+          acc[2 * e + 1] = fmaf(ws, __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
+        }
+      }
+      const int tok = Rs / G, h = g * G + Rs % G;
+      *reinterpret_cast<uint4*>(sg.out + (static_cast<size_t>(tok) * Hq + h) * D + dcol + k * 8) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                     pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+// CM: the most splits a launch of this build may merge in a cluster
+// (kMaxClusterSplits, or a small count whose combine keeps several rows'
+// loads in flight per thread).
+template <int D, int RING_KB, int CM = kMaxClusterSplits>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using Lay = Layout<D, RING_KB>;
   extern __shared__ uint8_t smem_raw[];
@@ -665,6 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
     __syncwarp();
     cluster_sync_all();   // release / acquire: the slots are visible to the whole cluster
+    if constexpr (CM < kMaxClusterSplits) {
+      // The build for clusters of at most CM splits: each CTA finishes many
+      // rows, so a thread takes several items per pass.
+      const int per = (kBM + C - 1) / C;
+      const int r0 = rank * per;
+      const int nr = max(0, min(per, kBM - r0));
+      cluster_combine<D, kMaxClusterSplits / CM, CM>(xo, xml, C, kPieces, r0, nr, mt, sg, p.Hq, p.G, g, dcol);
+    } else
     // Every thread of the CTA finishes at most one (piece k, row i) item per
     // pass, rows fastest (a warp's loads of one split are consecutive 16-byte
     // rows).  The C partial pieces and the C (m, l) of the row are loaded
@@ -805,16 +882,16 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
                  pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
 }
 
-template <int D, int RING_KB>
+template <int D, int RING_KB, int CM = kMaxClusterSplits>
 cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t s) {
   using Lay = Layout<D, RING_KB>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_kernel<D, RING_KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(attn_kernel<D, RING_KB, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Lay::ALLOC);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(attn_kernel<D, RING_KB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr_err = cudaFuncSetAttribute(attn_kernel<D, RING_KB, CM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (attr_err != cudaSuccess) return attr_err;
   dim3 grid(m_tiles, prm.n_splits, Hkv * prm.dparts);
@@ -834,10 +911,10 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, attn_kernel<D, RING_KB>, prm);
+    e = cudaLaunchKernelEx(&cfg, attn_kernel<D, RING_KB, CM>, prm);
     count_launch();
   } else {
-    e = launch_k(attn_kernel<D, RING_KB>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
+    e = launch_k(attn_kernel<D, RING_KB, CM>, grid, dim3(kThreads), Lay::ALLOC, s, prm);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1 || prm.fused) return e;
@@ -846,6 +923,19 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
                prm.seg[0].out, prm.seg[0].rows, prm.seg[0].m_tiles, prm.seg[1].out, prm.seg[1].rows,
                prm.n_splits, prm.dparts, prm.Hq, prm.G);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The build for head dimension D: the 128 KB ring for short key loops, else
+// the 160 KB ring with the merge for clusters of at most cm splits.
+template <int D>
+cudaError_t launch_d(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t s, bool deep, int cm) {
+  if (!deep) return launch_one<D, kRingShallowKB>(prm, m_tiles, Hkv, s);
+  switch (cm) {
+    case 2: return launch_one<D, kRingDeepKB, 2>(prm, m_tiles, Hkv, s);
+    case 4: return launch_one<D, kRingDeepKB, 4>(prm, m_tiles, Hkv, s);
+    case 8: return launch_one<D, kRingDeepKB, 8>(prm, m_tiles, Hkv, s);
+    default: return launch_one<D, kRingDeepKB>(prm, m_tiles, Hkv, s);
+  }
 }
 
 // How many clusters of c attention CTAs (one per SM) the device can hold at
@@ -1016,18 +1106,19 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   if (dparts != 1 && dparts != 2 && dparts != 4) return cudaErrorInvalidValue;
   if (a.D % (dparts * 64) != 0) return cudaErrorInvalidValue;
   const bool deep = (t_max + splits - 1) / splits > kShallowTiles;
+  // Long key loops merged by small clusters (many query tiles) get a build
+  // whose merge keeps several rows' loads in flight per thread.
+  const int cm = !(deep && fused) ? kMaxClusterSplits : splits <= 2 ? 2 : splits <= 4 ? 4 : splits <= 8 ? 8
+                                                                                             : kMaxClusterSplits;
   prm.n_splits = splits;
   prm.dparts = dparts;
   prm.inject_tx = a.inject_tx;
   prm.fused = fused ? 1 : 0;
   if (used_splits) *used_splits = splits;
   switch (a.D) {
-    case 64: return deep ? launch_one<64, kRingDeepKB>(prm, m_total, a.Hkv, s)
-                         : launch_one<64, kRingShallowKB>(prm, m_total, a.Hkv, s);
-    case 128: return deep ? launch_one<128, kRingDeepKB>(prm, m_total, a.Hkv, s)
-                          : launch_one<128, kRingShallowKB>(prm, m_total, a.Hkv, s);
-    case 256: return deep ? launch_one<256, kRingDeepKB>(prm, m_total, a.Hkv, s)
-                          : launch_one<256, kRingShallowKB>(prm, m_total, a.Hkv, s);
+    case 64: return launch_d<64>(prm, m_total, a.Hkv, s, deep, cm);
+    case 128: return launch_d<128>(prm, m_total, a.Hkv, s, deep, cm);
+    case 256: return launch_d<256>(prm, m_total, a.Hkv, s, deep, cm);
     default: return cudaErrorInvalidValue;
   }
 }

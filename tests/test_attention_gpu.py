@@ -326,6 +326,31 @@ def test_long_key_loop_separate_k_and_v_rings(rx, D, dparts):
     cache.close()
 
 
+@pytest.mark.parametrize("D,dparts,splits,S", [(64, 1, 2, 250), (128, 2, 2, 250), (256, 1, 2, 250),
+                                                (256, 2, 2, 250), (256, 1, 3, 250), (128, 1, 4, 250),
+                                                (256, 2, 5, 120), (256, 1, 6, 120), (64, 1, 8, 120)])
+def test_small_cluster_builds_long_suffix(rx, D, dparts, splits, S):
+    """Long key loops merged by clusters of at most 2, 4 or 8 splits (a long
+    suffix over a short window) run builds whose merge takes several rows
+    per thread and pass.  250 or 120 tokens x 8 heads leave a ragged last
+    query tile."""
+    wl = W.Workload("small-cluster-d%d" % D, L=1, Hq=8, Hkv=1, D=D, P=64, N=8, F=256, S=S, steps=1, ticks=1,
+                    d_model=128, emb_dim=16, state_dim=16, hidden=64)
+    seed = 41 + D + dparts + splits
+    cache = _make(rx, wl, seed)
+    cache.set_attn_splits(splits)
+    cache.set_attn_dparts(dparts)
+    ost = OracleStream(wl, seed)
+    for t in range(wl.N + 1):
+        fk, fv = W.frame_kv(wl, seed, t)
+        cache.push_frame(dev(fk), dev(fv))
+        ost.push(t)
+    got = host64(_attend(cache, wl, seed, wl.N, 0, 0))
+    check_attention(got, _oracle_attend(ost, wl, seed, wl.N, 0, 0))
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
 def test_2048_token_suffix_one_split_per_tile(rx):
     """A 2048-token suffix over an 8-frame window (16384 query rows, 128 query
     tiles, 4160 keys): the automatic partition gives every query tile one CTA
