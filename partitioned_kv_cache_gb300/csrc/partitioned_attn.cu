@@ -72,6 +72,7 @@ constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a 
 constexpr int kRingShallowKB = 128;
 constexpr int kRingDeepKB = 160;
 constexpr int kShallowTiles = 4;
+constexpr int kMergeWide = 32;               // build tag: see attn_kernel's CM
 
 template <int D, int RING_KB>
 struct Layout {
@@ -222,36 +223,38 @@ __device__ __forceinline__ float2* xchg_ml(const AttnParams& p, int DV, int spli
 }
 
 // The cluster merge's last step: rows [r0, r0 + nr) of the tile from the C
-// partial slots of the cluster.  Items are (piece k, row i) pairs, rows
-// fastest (a warp's loads of one split are consecutive 16-byte rows).  Each
-// thread takes U items per pass and loads the CM >= C partial pieces and
-// (m, l) of each together, U * CM = 16 loads in flight (splits >= C re-read
-// split C-1 and weigh 0).  The weight of split s is 2^(m_s - M) l_s / sum, as
-// the partials are O_s / l_s.
-template <int D, int U, int CM>
+// partial slots of the cluster.  An item is PP adjacent 16-byte pieces of one
+// row; items go rows fastest (a warp's loads of one split are consecutive
+// 16-byte rows).  Each thread takes U items per pass and loads the CM >= C
+// partial pieces and (m, l) of each together (splits >= C re-read split C-1
+// and weigh 0), U * CM * PP pieces in flight.  The weight of split s is
+// 2^(m_s - M) l_s / sum, as the partials are O_s / l_s.
+template <int D, int U, int CM, int PP = 1>
 __device__ __forceinline__ void cluster_combine(const uint4* xo, const float2* xml, int C, int kPieces, int r0,
                                                 int nr, int mt, const SegParams& sg, int Hq, int G, int g,
                                                 int dcol) {
-  const int items = nr * kPieces;
+  const int items = nr * (kPieces / PP);
   for (int base = threadIdx.x; base < items; base += kThreads * U) {
-    uint4 pv[U][CM];
+    uint4 pv[U][PP][CM];
     float2 ml[U][CM];
 #pragma unroll
     for (int q = 0; q < U; ++q) {
       const int item = min(base + q * kThreads, items - 1);   // past the end: re-read, not stored
-      const int i = item % nr, k = item / nr;
+      const int i = item % nr, k = item / nr * PP;
       const uint4* src = xo + static_cast<size_t>(k) * kBM + r0 + i;
 #pragma unroll
       for (int s2 = 0; s2 < CM; ++s2) {
         const int sc = min(s2, C - 1);
-        pv[q][s2] = __ldcg(src + static_cast<size_t>(sc) * kPieces * kBM);
+#pragma unroll
+        for (int pp = 0; pp < PP; ++pp)
+          pv[q][pp][s2] = __ldcg(src + static_cast<size_t>(sc) * kPieces * kBM + pp * kBM);
         ml[q][s2] = __ldcg(xml + sc * kBM + r0 + i);
       }
     }
 #pragma unroll
     for (int q = 0; q < U; ++q) {
       const int item = base + q * kThreads;
-      const int i = item % nr, k = item / nr;
+      const int i = item % nr, k = item / nr * PP;
       const int Rs = mt * kBM + r0 + i;
       if (item >= items || Rs >= sg.rows) continue;
       float M = -INFINITY;
@@ -266,30 +269,35 @@ __device__ __forceinline__ void cluster_combine(const uint4* xo, const float2* x
         L += w[s2];
       }
       const float invL = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < CM; ++s2) {
-        const float ws = w[s2] * invL;
-        const uint32_t vv[4] = {pv[q][s2].x, pv[q][s2].y, pv[q][s2].z, pv[q][s2].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[2 * e] = fmaf(ws, __uint_as_float(vv[e] << 16), acc[2 * e]);
-          acc[2 * e + 1] = fmaf(ws, __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
-        }
-      }
       const int tok = Rs / G, h = g * G + Rs % G;
-      *reinterpret_cast<uint4*>(sg.out + (static_cast<size_t>(tok) * Hq + h) * D + dcol + k * 8) =
-          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                     pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+      for (int pp = 0; pp < PP; ++pp) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < CM; ++s2) {
+          const float ws = w[s2] * invL;
+          const uint32_t vv[4] = {pv[q][pp][s2].x, pv[q][pp][s2].y, pv[q][pp][s2].z, pv[q][pp][s2].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = fmaf(ws, __uint_as_float(vv[e] << 16), acc[2 * e]);
+            acc[2 * e + 1] = fmaf(ws, __uint_as_float(vv[e] & 0xFFFF0000u), acc[2 * e + 1]);
+          }
+        }
+        *reinterpret_cast<uint4*>(sg.out + (static_cast<size_t>(tok) * Hq + h) * D + dcol + (k + pp) * 8) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                       pack_bf16x2(acc[6], acc[7]));
+      }
     }
   }
 }
 
 // CM: the most splits a launch of this build may merge in a cluster
 // (kMaxClusterSplits, or a small count whose combine keeps several rows'
-// loads in flight per thread).
+// loads in flight per thread), or kMergeWide: up to kMaxClusterSplits splits
+// whose rows hold more (row, piece) items than the CTA has threads, taken two
+// pieces per thread so that one pass finishes them.
 template <int D, int RING_KB, int CM = kMaxClusterSplits>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using Lay = Layout<D, RING_KB>;
@@ -734,7 +742,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
     __syncwarp();
     cluster_sync_all();   // release / acquire: the slots are visible to the whole cluster
-    if constexpr (CM < kMaxClusterSplits) {
+    if constexpr (CM == kMergeWide) {
+      const int per = (kBM + C - 1) / C;
+      const int r0 = rank * per;
+      const int nr = max(0, min(per, kBM - r0));
+      cluster_combine<D, 1, kMaxClusterSplits, 2>(xo, xml, C, kPieces, r0, nr, mt, sg, p.Hq, p.G, g, dcol);
+    } else if constexpr (CM < kMaxClusterSplits) {
       // The build for clusters of at most CM splits: each CTA finishes many
       // rows, so a thread takes several items per pass.
       const int per = (kBM + C - 1) / C;
@@ -926,11 +939,15 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
 }
 
 // The build for head dimension D: the 128 KB ring for short key loops, else
-// the 160 KB ring with the merge for clusters of at most cm splits.
+// the 160 KB ring; with the merge for clusters of at most cm splits, or the
+// two-pieces-per-thread merge (cm = kMergeWide).
 template <int D>
 cudaError_t launch_d(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t s, bool deep, int cm) {
-  if (!deep) return launch_one<D, kRingShallowKB>(prm, m_tiles, Hkv, s);
+  if (!deep)
+    return cm == kMergeWide ? launch_one<D, kRingShallowKB, kMergeWide>(prm, m_tiles, Hkv, s)
+                            : launch_one<D, kRingShallowKB>(prm, m_tiles, Hkv, s);
   switch (cm) {
+    case kMergeWide: return launch_one<D, kRingDeepKB, kMergeWide>(prm, m_tiles, Hkv, s);
     case 2: return launch_one<D, kRingDeepKB, 2>(prm, m_tiles, Hkv, s);
     case 4: return launch_one<D, kRingDeepKB, 4>(prm, m_tiles, Hkv, s);
     case 8: return launch_one<D, kRingDeepKB, 8>(prm, m_tiles, Hkv, s);
@@ -1108,8 +1125,12 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   const bool deep = (t_max + splits - 1) / splits > kShallowTiles;
   // Long key loops merged by small clusters (many query tiles) get a build
   // whose merge keeps several rows' loads in flight per thread.
-  const int cm = !(deep && fused) ? kMaxClusterSplits : splits <= 2 ? 2 : splits <= 4 ? 4 : splits <= 8 ? 8
-                                                                                             : kMaxClusterSplits;
+  // Clusters whose CTAs each finish more (row, piece) items than they have
+  // threads get the build that takes two pieces per thread.
+  const int merge_items = (kBM + splits - 1) / splits * (a.D / dparts / 8);
+  const int cm = !fused ? kMaxClusterSplits
+                 : deep && splits <= 2 ? 2 : deep && splits <= 4 ? 4 : deep && splits <= 8 ? 8
+                 : merge_items > kThreads ? kMergeWide : kMaxClusterSplits;
   prm.n_splits = splits;
   prm.dparts = dparts;
   prm.inject_tx = a.inject_tx;
