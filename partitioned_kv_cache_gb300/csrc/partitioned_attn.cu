@@ -753,7 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       const int per = (kBM + C - 1) / C;
       const int r0 = rank * per;
       const int nr = max(0, min(per, kBM - r0));
-      cluster_combine<D, kMaxClusterSplits / CM, CM>(xo, xml, C, kPieces, r0, nr, mt, sg, p.Hq, p.G, g, dcol);
+      // Two pieces of a row per item (one (m, l) load for both), and enough
+      // items per thread that the 64, 32 or 22 rows x 32 pieces of a
+      // cluster of 2, 4 or 6-8 splits at D = 256 take one pass.
+      constexpr int kU = CM == 2 ? 5 : CM == 4 ? 3 : 2;
+      cluster_combine<D, kU, CM, 2>(xo, xml, C, kPieces, r0, nr, mt, sg, p.Hq, p.G, g, dcol);
     } else
     // Every thread of the CTA finishes at most one (piece k, row i) item per
     // pass, rows fastest (a warp's loads of one split are consecutive 16-byte
