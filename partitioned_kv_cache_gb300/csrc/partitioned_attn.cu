@@ -64,11 +64,12 @@ namespace {
 constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a cluster
-// Shared memory for the K/V ring.  Two builds of the kernel: 128 KB for key
-// loops of at most kShallowTiles tiles per CTA, which have nothing to gain
-// from a deeper ring and run faster with the smaller allocation, and 160 KB
-// for longer loops, which prefetch one tile deeper and split it into a K ring
-// (3/5 of it) and a V ring.
+// Shared memory for the K/V ring, in two sizes (separate builds of the
+// kernel, each also built per merge shape; see attn_kernel's CM): 128 KB for
+// key loops of at most kShallowTiles tiles per CTA, which have nothing to
+// gain from a deeper ring and run faster with the smaller allocation, and
+// 160 KB for longer loops, which prefetch one tile deeper and split it into
+// a K ring (3/5 of it) and a V ring.
 constexpr int kRingShallowKB = 128;
 constexpr int kRingDeepKB = 160;
 constexpr int kShallowTiles = 4;
