@@ -825,12 +825,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // Combine the splits of every row when they do not form a cluster (more than
 // kMaxClusterSplits of them), over the exchange area the attention grid
 // wrote, with the weighting of the in-kernel merge: out = sum_s w_s O_s / l_s
-// divided by sum_s w_s, where w_s = 2^(m_s - M) l_s.  One thread per (row,
-// 16-byte piece), rows fastest, so a warp's load of one split is 512
-// contiguous bytes.  Grid: (M-tiles of all segments, pieces / 2, Hkv x dparts),
-// the attention grid's x and z.  The splits are taken 16 at a time, their
-// loads in flight together, with a running maximum: a chunk that raises it
-// rescales the sums so far.
+// divided by sum_s w_s, where w_s = 2^(m_s - M) l_s.  A lane pair owns one
+// (row, 16-byte piece): lane 2r + h takes the splits s = h, h + 2, ...  A
+// warp covers 16 consecutive rows of one piece, so its load of one split
+// pair is two runs of 256 contiguous bytes.  Grid: (M-tiles of all segments,
+// pieces, Hkv x dparts), the attention grid's x and z, with 256 threads = 128
+// rows.  Each lane loads up to 16 of its splits at a time, so up to 32 splits
+// are in flight per (row, piece).  More splits run with a running maximum.
+// The pair's (M, L, sums) meet by one shuffle.
 constexpr int kCombineChunk = 16;
 
 template <int D>
@@ -846,10 +848,12 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
   const int mt = blockIdx.x - (si ? m_tiles0 : 0);
   const int rows = si ? rows1 : rows0;
   __nv_bfloat16* out = si ? out1 : out0;
-  const int i = threadIdx.x & (kBM - 1);
-  const int k = blockIdx.y * 2 + (threadIdx.x >> 7);
+  const int lane = threadIdx.x & 31;
+  const int half = lane & 1;
+  const int i = (threadIdx.x >> 5) * 16 + (lane >> 1);   // row within the tile
+  const int k = blockIdx.y;                                // piece
   const int Rs = mt * kBM + i;
-  if (Rs >= rows) return;   // padding rows were never written
+  const bool live_row = Rs < rows;   // padding rows were never written: their loads stay in the tile
   const int C = n_splits;
   const size_t cid = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
   const uint4* src = xchg + cid * C * kPieces * kBM + static_cast<size_t>(k) * kBM + i;
@@ -860,20 +864,21 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < C; s0 += kCombineChunk) {
+  for (int s0 = half; s0 < C; s0 += 2 * kCombineChunk) {
     uint4 pv[kCombineChunk];
     float2 ml[kCombineChunk];
 #pragma unroll
-    for (int u = 0; u < kCombineChunk; ++u) {   // past the last split: re-read it, weigh 0
-      const int sc = min(s0 + u, C - 1);
-      pv[u] = __ldcg(src + static_cast<size_t>(sc) * kPieces * kBM);
-      ml[u] = __ldcg(ml_src + static_cast<size_t>(sc) * kBM);
+    for (int u = 0; u < kCombineChunk; ++u) {   // this lane's splits s0, s0 + 2, ...
+      const int s = s0 + 2 * u;
+      const bool use = live_row && s < C;
+      pv[u] = use ? __ldcg(src + static_cast<size_t>(s) * kPieces * kBM) : make_uint4(0u, 0u, 0u, 0u);
+      ml[u] = use ? __ldcg(ml_src + static_cast<size_t>(s) * kBM) : make_float2(-INFINITY, 0.f);
     }
     float mc = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kCombineChunk; ++u)
-      if (s0 + u < C && ml[u].y > 0.f) mc = fmaxf(mc, ml[u].x);
-    if (mc == -INFINITY) continue;   // no split of this chunk saw a key
+      if (ml[u].y > 0.f) mc = fmaxf(mc, ml[u].x);
+    if (mc == -INFINITY) continue;   // none of these splits saw a key
     const float Mn = fmaxf(M, mc);
     const float sc = exp2f(M - Mn);  // 0 before the first live split
     L *= sc;
@@ -881,7 +886,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
     for (int e = 0; e < 8; ++e) acc[e] *= sc;
 #pragma unroll
     for (int u = 0; u < kCombineChunk; ++u) {
-      const float w = s0 + u < C && ml[u].y > 0.f ? exp2f(ml[u].x - Mn) * ml[u].y : 0.f;
+      const float w = ml[u].y > 0.f ? exp2f(ml[u].x - Mn) * ml[u].y : 0.f;
       L += w;
       const uint32_t vv[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
 #pragma unroll
@@ -892,6 +897,18 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
     }
     M = Mn;
   }
+  // The lane pair's halves: rescale both to the larger maximum and add.
+  const float Mo = __shfl_xor_sync(0xffffffffu, M, 1);
+  const float Mt = fmaxf(M, Mo);
+  const float f = M == -INFINITY ? 0.f : exp2f(M - Mt);
+  L *= f;
+  L += __shfl_xor_sync(0xffffffffu, L, 1);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    acc[e] *= f;
+    acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 1);
+  }
+  if (half || !live_row) return;
   const float inv = L > 0.f ? 1.f / L : 0.f;   // a row with no key at all gets zeros
   const int g = blockIdx.z / dparts, dcol = (blockIdx.z % dparts) * DV;
   const int tok = Rs / G, h = g * G + Rs % G;
@@ -936,7 +953,7 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1 || prm.fused) return e;
-  dim3 cgrid(m_tiles, D / prm.dparts / 16, Hkv * prm.dparts);
+  dim3 cgrid(m_tiles, D / prm.dparts / 8, Hkv * prm.dparts);
   e = launch_k(attn_combine_kernel<D>, cgrid, dim3(256), 0, s, static_cast<const uint4*>(prm.xchg),
                prm.seg[0].out, prm.seg[0].rows, prm.seg[0].m_tiles, prm.seg[1].out, prm.seg[1].rows,
                prm.n_splits, prm.dparts, prm.Hq, prm.G);
@@ -1009,6 +1026,18 @@ double split_cost(int t_max, int splits, int dparts) {
   double c = tiles * (1.0 + 0.2 / dparts);
   if (splits > 1) c += 3.0 / dparts + 2.5;
   return c;
+}
+
+// The same units for more splits than one cluster, merged by
+// attn_combine_kernel after the grid: 1.2 a key tile of the longest split
+// plus 7.3 for the exchange, the second launch and its combine.  Fitted to
+// 2163-, 4352-, 6400- and 8448-key suffixes: the unclustered merge won
+// wherever the cluster left 5 or more tiles per split (8448 keys: 13.55
+// against 15.12 us; 4352: 11.04 against 11.42 us) and lost at 3 (c3 and the
+// shared-cache batch: 9.09 against 8.82 us, 11.23 against 11.12 us).
+double split_cost_unclustered(int t_max, int splits) {
+  const int tiles = (t_max + splits - 1) / splits;
+  return tiles * 1.2 + 7.3;
 }
 
 }  // namespace
@@ -1116,6 +1145,17 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
           bs = sp;
           bd = dp;
         }
+      }
+    }
+    // More splits than a cluster holds, merged by attn_combine_kernel: as
+    // many as keep the grid within three quarters of the SMs.
+    const int sp_nf = min(min(t_max, a.max_splits), 3 * a.num_sms / 4 / max(units, 1));
+    if (sp_nf > kMaxClusterSplits && (splits == 0 || splits == sp_nf) && dparts <= 1) {
+      const double c = split_cost_unclustered(t_max, sp_nf);
+      if (c < best - 1e-9) {
+        best = c;
+        bs = sp_nf;
+        bd = 1;
       }
     }
     if (splits == 0) splits = bs;
