@@ -73,7 +73,8 @@ constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a 
 constexpr int kRingShallowKB = 128;
 constexpr int kRingDeepKB = 160;
 constexpr int kShallowTiles = 4;
-constexpr int kMergeWide = 32;               // build tag: see attn_kernel's CM
+constexpr int kMergeWide = 32;               // build tags: see attn_kernel's CM
+constexpr int kNoClusterMerge = 0;
 
 template <int D, int RING_KB>
 struct Layout {
@@ -298,7 +299,8 @@ __device__ __forceinline__ void cluster_combine(const uint4* xo, const float2* x
 // (kMaxClusterSplits, or a small count whose combine keeps several rows'
 // loads in flight per thread), or kMergeWide: up to kMaxClusterSplits splits
 // whose rows hold more (row, piece) items than the CTA has threads, taken two
-// pieces per thread so that one pass finishes them.
+// pieces per thread so that one pass finishes them; or kNoClusterMerge, for
+// launches whose splits are merged by attn_combine_kernel.
 template <int D, int RING_KB, int CM = kMaxClusterSplits>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using Lay = Layout<D, RING_KB>;
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
   }
 
-  if (p.fused) {
+  if constexpr (CM != kNoClusterMerge) if (p.fused) {
     // ---------------------------------------------------------- cluster merge
     // The C splits of this (tile, head, column share) exchange their partials
     // through L2: each softmax thread writes its row's normalised partial
@@ -969,6 +971,7 @@ cudaError_t launch_d(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t s
     return cm == kMergeWide ? launch_one<D, kRingShallowKB, kMergeWide>(prm, m_tiles, Hkv, s)
                             : launch_one<D, kRingShallowKB>(prm, m_tiles, Hkv, s);
   switch (cm) {
+    case kNoClusterMerge: return launch_one<D, kRingDeepKB, kNoClusterMerge>(prm, m_tiles, Hkv, s);
     case kMergeWide: return launch_one<D, kRingDeepKB, kMergeWide>(prm, m_tiles, Hkv, s);
     case 2: return launch_one<D, kRingDeepKB, 2>(prm, m_tiles, Hkv, s);
     case 4: return launch_one<D, kRingDeepKB, 4>(prm, m_tiles, Hkv, s);
@@ -1173,7 +1176,7 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   // Clusters whose CTAs each finish more (row, piece) items than they have
   // threads get the build that takes two pieces per thread.
   const int merge_items = (kBM + splits - 1) / splits * (a.D / dparts / 8);
-  const int cm = !fused ? kMaxClusterSplits
+  const int cm = !fused ? (splits > 1 ? kNoClusterMerge : kMaxClusterSplits)
                  : deep && splits <= 2 ? 2 : deep && splits <= 4 ? 4 : deep && splits <= 8 ? 8
                  : merge_items > kThreads ? kMergeWide : kMaxClusterSplits;
   prm.n_splits = splits;
