@@ -284,6 +284,25 @@ rx_status rx_check_device_error(rx_cache_t cache, int* code, void* stream);
  * Errors: RX_ERR_ARG. */
 rx_status rx_debug_inject_timeout(rx_cache_t cache, int bytes);
 
+/* Test aid: the partition an attention launch chooses, computed on the host
+ * from the given device figures.  Proposition A.1 of "Reflex: Real-Time VLA
+ * Control through Streaming Inference" (§III "Core formulas") lets the key
+ * sequence be cut into slices merged afterwards.  A launch runs `units` =
+ * (128-row query tiles x K/V heads).  Each is cut into *splits key slices
+ * times *dparts output-column shares.  *fused = 1 when the splits of a unit
+ * form one thread-block cluster and merge on chip, 0 when a second kernel
+ * merges them (or *splits = 1).  Inputs: t_max = key tiles (64 keys) of the
+ * longest query segment; D = 64, 128 or 256; num_sms; max_splits = splits
+ * the cache's workspace holds; forced_splits / forced_dparts = 0 for the
+ * automatic choice (as rx_set_attn_splits / rx_set_attn_dparts);
+ * cluster_capacity = host array of 17 ints, entry c = clusters of c CTAs the
+ * device holds at once (entry 0 unused).  Touches no device.
+ * Errors: RX_ERR_ARG (a size below 1, a null pointer, or a column split that
+ * is not 1, 2 or 4 or leaves a share narrower than 64 columns). */
+rx_status rx_debug_choose_partition(int t_max, int units, int D, int num_sms, int max_splits,
+                                    int forced_splits, int forced_dparts, const int* cluster_capacity,
+                                    int* splits, int* dparts, int* fused);
+
 /* Number of split-KV partitions for attention launches of this cache
  * (0 = chosen from the SM count, the default).  A tuning knob: results are
  * the same for every value up to rounding order. */

@@ -55,6 +55,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "partition.h"
 #include "rx_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -63,7 +64,6 @@ namespace {
 
 constexpr int kThreads = 224;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kMaxClusterSplits = 16;        // splits merged on chip through a cluster
 // Shared memory for the K/V ring, in two sizes (separate builds of the
 // kernel, each also built per merge shape; see attn_kernel's CM): 128 KB for
 // key loops of at most kShallowTiles tiles per CTA, which have nothing to
@@ -1015,34 +1015,6 @@ const int* cluster_capacity() {
   return cap;
 }
 
-// Relative cost of one launch, in units of about 0.7 us on GB300: each key
-// tile of the longest split costs 1 + 0.2/dparts (the K tile, the S tile
-// and the softmax chain are the same for every column share; only the V
-// bytes and the P V product shrink), and a cluster merge costs 3/dparts for
-// the partials' exchange through L2 plus 2.5 for its barrier and combine.
-// Fitted to timings of 2163- and 8448-key suffixes and the shared-cache batch
-// (12 x 2, 16 x 1 and 16 x 1 win there).  Ties go to more splits: the longest
-// split is as long, but the average one is shorter (8448 keys: 16 x 1 is
-// 0.4 us faster than 15 x 1; the batch: 16 x 1 0.3 us faster than 14 x 1).
-double split_cost(int t_max, int splits, int dparts) {
-  const int tiles = (t_max + splits - 1) / splits;
-  double c = tiles * (1.0 + 0.2 / dparts);
-  if (splits > 1) c += 3.0 / dparts + 2.5;
-  return c;
-}
-
-// The same units for more splits than one cluster, merged by
-// attn_combine_kernel after the grid: 1.2 a key tile of the longest split
-// plus 7.3 for the exchange, the second launch and its combine.  Fitted to
-// 2163-, 4352-, 6400- and 8448-key suffixes: the unclustered merge won
-// wherever the cluster left 5 or more tiles per split (8448 keys: 13.55
-// against 15.12 us; 4352: 11.04 against 11.42 us) and lost at 3 (c3 and the
-// shared-cache batch: 9.09 against 8.82 us, 11.23 against 11.12 us).
-double split_cost_unclustered(int t_max, int splits) {
-  const int tiles = (t_max + splits - 1) / splits;
-  return tiles * 1.2 + 7.3;
-}
-
 }  // namespace
 
 cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment* segs, int nseg,
@@ -1113,10 +1085,9 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   prm.G = G;
   prm.rows_pad = m_total * kBM;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
-  // Partition: `splits` slices of the key sequence (a cluster that merges on
-  // chip) times `dparts` shares of the output columns per (tile, head).  The
-  // automatic choice minimises split_cost over the partitions whose clusters
-  // all fit on the device at once (one wave).
+  // Partition (partition.h): `splits` slices of the key sequence times
+  // `dparts` shares of the output columns per (tile, head), from the
+  // device's cluster capacity.
   const int* cap = nullptr;
   switch (a.D) {
     case 64: cap = cluster_capacity<64, kRingDeepKB>(); break;   // the larger build: capacity it fits
@@ -1125,51 +1096,11 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
     default: return cudaErrorInvalidValue;
   }
   const int units = m_total * a.Hkv;
-  // A cluster merge exchanges its partials through the workspace, which
-  // holds at most max_splits of them.
-  auto fits = [&](int sp, int dp) {
-    if (sp == 1) return units * dp <= a.num_sms;
-    return sp <= kMaxClusterSplits && sp <= a.max_splits && units * dp <= cap[sp];
-  };
-  int splits = a.forced_splits > 0 ? a.forced_splits : 0;
-  int dparts = a.forced_dparts > 0 ? a.forced_dparts : 0;
-  if (splits == 0 || dparts == 0) {
-    double best = 1e30;
-    int bs = 1, bd = 1;
-    const int s_hi = t_max < kMaxClusterSplits ? t_max : kMaxClusterSplits;
-    for (int sp = 1; sp <= s_hi; ++sp) {
-      if (splits > 0 && sp != splits) continue;
-      for (int dp = 1; dp <= 4; dp *= 2) {
-        if (dparts > 0 && dp != dparts) continue;
-        if (a.D / dp < 64 || !fits(sp, dp)) continue;
-        const double c = split_cost(t_max, sp, dp);
-        if (c < best - 1e-9 || (c < best + 1e-9 && sp > bs)) {
-          best = c;
-          bs = sp;
-          bd = dp;
-        }
-      }
-    }
-    // More splits than a cluster holds, merged by attn_combine_kernel: as
-    // many as keep the grid within three quarters of the SMs.
-    const int sp_nf = min(min(t_max, a.max_splits), 3 * a.num_sms / 4 / max(units, 1));
-    if (sp_nf > kMaxClusterSplits && (splits == 0 || splits == sp_nf) && dparts <= 1) {
-      const double c = split_cost_unclustered(t_max, sp_nf);
-      if (c < best - 1e-9) {
-        best = c;
-        bs = sp_nf;
-        bd = 1;
-      }
-    }
-    if (splits == 0) splits = bs;
-    if (dparts == 0) dparts = bd;
-  }
-  splits = splits > t_max ? t_max : splits;
-  splits = splits > a.max_splits ? a.max_splits : splits;
-  splits = splits < 1 ? 1 : splits;
-  const bool fused = splits >= 2 && splits <= kMaxClusterSplits && cap[splits] >= 1;
-  if (dparts != 1 && dparts != 2 && dparts != 4) return cudaErrorInvalidValue;
-  if (a.D % (dparts * 64) != 0) return cudaErrorInvalidValue;
+  PartitionChoice pc;
+  if (!choose_partition({t_max, units, a.D, a.num_sms, a.max_splits, a.forced_splits, a.forced_dparts, cap}, &pc))
+    return cudaErrorInvalidValue;
+  const int splits = pc.splits, dparts = pc.dparts;
+  const bool fused = pc.fused;
   const bool deep = (t_max + splits - 1) / splits > kShallowTiles;
   // Long key loops merged by small clusters (many query tiles) get a build
   // whose merge keeps several rows' loads in flight per thread.

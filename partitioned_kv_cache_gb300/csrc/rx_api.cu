@@ -23,6 +23,7 @@
 #include <string>
 
 #include "rx.h"
+#include "partition.h"
 #include "rx_internal.h"
 
 namespace {
@@ -686,6 +687,26 @@ rx_status rx_debug_inject_timeout(rx_cache_t h, int bytes) {
   if (bytes < 0 || bytes > (1 << 20) || (bytes & 15))
     return fail(RX_ERR_ARG, "rx_debug_inject_timeout: %d not a multiple of 16 in [0, 2^20]", bytes);
   h->inject_tx = bytes;
+  return RX_OK;
+  RX_GUARD_END
+}
+
+rx_status rx_debug_choose_partition(int t_max, int units, int D, int num_sms, int max_splits,
+                                    int forced_splits, int forced_dparts, const int* cluster_capacity,
+                                    int* splits, int* dparts, int* fused) {
+  RX_GUARD_BEGIN
+  if (!cluster_capacity || !splits || !dparts || !fused)
+    return fail(RX_ERR_ARG, "rx_debug_choose_partition: null pointer");
+  if (t_max < 1 || units < 1 || num_sms < 1 || max_splits < 1 || forced_splits < 0 || forced_dparts < 0)
+    return fail(RX_ERR_ARG, "rx_debug_choose_partition: sizes out of range");
+  if (D != 64 && D != 128 && D != 256) return fail(RX_ERR_ARG, "rx_debug_choose_partition: D = %d", D);
+  rx::PartitionChoice pc;
+  if (!rx::choose_partition({t_max, units, D, num_sms, max_splits, forced_splits, forced_dparts, cluster_capacity},
+                            &pc))
+    return fail(RX_ERR_ARG, "rx_debug_choose_partition: column split %d does not fit D = %d", forced_dparts, D);
+  *splits = pc.splits;
+  *dparts = pc.dparts;
+  *fused = pc.fused ? 1 : 0;
   return RX_OK;
   RX_GUARD_END
 }

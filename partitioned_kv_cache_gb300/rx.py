@@ -31,7 +31,7 @@ EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_fram
            "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
            "rx_attend_regions_static", "rx_attend_suffix_block_causal", "rx_tail_append",
            "rx_snapshot_bytes", "rx_snapshot", "rx_restore", "rx_push_frame_async",
-           "rx_set_attn_dparts", "rx_debug_inject_timeout")
+           "rx_set_attn_dparts", "rx_debug_inject_timeout", "rx_debug_choose_partition")
 
 
 class RxConfig(ctypes.Structure):
@@ -64,6 +64,8 @@ _sigs = {
     "rx_set_attn_splits": (_i, [_vp, _i]),
     "rx_set_attn_dparts": (_i, [_vp, _i]),
     "rx_debug_inject_timeout": (_i, [_vp, _i]),
+    "rx_debug_choose_partition": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i),
+                                       ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "rx_launch_count": (ctypes.c_longlong, []),
     "rx_status_str": (ctypes.c_char_p, [_i]),
     "rx_last_error": (ctypes.c_char_p, []),
@@ -114,6 +116,19 @@ def _ptr(t: Optional[torch.Tensor], dtype=torch.bfloat16, name: str = "tensor",
 
 def launch_count() -> int:
     return int(_lib.rx_launch_count())
+
+
+def choose_partition(t_max: int, units: int, D: int, num_sms: int, max_splits: int,
+                     cluster_capacity, splits: int = 0, dparts: int = 0):
+    """Test aid: (splits, dparts, fused) of an attention launch, computed on
+    the host from the given device figures (rx_debug_choose_partition).
+    cluster_capacity: 17 ints, entry c = clusters of c CTAs the device holds."""
+    cap = (_i * 17)(*[int(c) for c in cluster_capacity])
+    sp, dp, fu = _i(0), _i(0), _i(0)
+    _check(_lib.rx_debug_choose_partition(t_max, units, D, num_sms, max_splits, splits, dparts, cap,
+                                          ctypes.byref(sp), ctypes.byref(dp), ctypes.byref(fu)),
+           "rx_debug_choose_partition")
+    return sp.value, dp.value, bool(fu.value)
 
 
 def library_path() -> str:
