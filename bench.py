@@ -132,23 +132,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.out.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
-            except ValueError:
-                continue
+        with open(self.path) as f:
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower().startswith("active")})
-        sm = sorted(r[0] for r in rows)
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return summarise_clock_rows(lines)
+
+
+def summarise_clock_rows(lines):
+    """The clocks entry of the JSON line from nvidia-smi rows in
+    ClockSampler.FIELDS order (csv, no header, no units): the median SM clock
+    under load, the largest maximum clock seen, and every throttle reason
+    that was active in any sample.  Rows that do not parse (an "[N/A]" clock,
+    a short line) are skipped; no usable row gives None."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower().startswith("active")})
+    sm = sorted(r[0] for r in rows)
+    return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows)}
 
 
 # ---------------------------------------------------------------------------

@@ -43,3 +43,19 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_clock_record_from_nvidia_smi_rows():
+    """The clocks entry that decides whether a timed run is kept: the median
+    SM clock, the maximum, and every throttle reason active in any sample."""
+    import bench
+    idle = "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+    capped = "0, 1965, 2070, 1398.7, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+    thermal = "0, 1500, 2070, 1200.0, 0x0000000000000020, Not Active, Active, Not Active, Not Active\n"
+    bad = ["0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active\n", "garbage\n", "\n"]
+    r = bench.summarise_clock_rows([idle, idle, capped] + bad)
+    assert r == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    r = bench.summarise_clock_rows([idle, thermal, thermal, capped])
+    assert r["sm_mhz"] == 1965.0 and r["samples"] == 4
+    assert r["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.summarise_clock_rows(bad) is None
