@@ -92,3 +92,20 @@ def test_cache_calls_reject_null_handle(lib):
     assert L.rx_set_attn_splits(None, 0) == -1
     assert L.rx_set_attn_dparts(None, 0) == -1
     assert L.rx_debug_inject_timeout(None, 16) == -1
+
+
+def test_binding_checks_tensors_before_calling_the_library(lib):
+    """rx.py only marshals arguments: a wrong dtype, a strided view or a host
+    tensor is refused in Python, before any C call (CPU only)."""
+    import torch
+    from partitioned_kv_cache_gb300 import rx
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    g = torch.ones(64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        rx.adarmsnorm(x.float(), g, 1e-6)                  # fp32 input
+    with pytest.raises(ValueError):
+        rx.adarmsnorm(torch.zeros(64, 8, dtype=torch.bfloat16).t(), g, 1e-6)   # not contiguous
+    with pytest.raises(ValueError):
+        rx.adarmsnorm(x, g, 1e-6)                          # host memory
+    with pytest.raises(rx.RxError):
+        rx.choose_partition(34, 4, 96, 152, 64, [0] * 17)  # head dimension 96
