@@ -297,8 +297,9 @@ rx_status rx_debug_inject_timeout(rx_cache_t cache, int bytes);
  * automatic choice (as rx_set_attn_splits / rx_set_attn_dparts);
  * cluster_capacity = host array of 17 ints, entry c = clusters of c CTAs the
  * device holds at once (entry 0 unused).  Touches no device.
- * Errors: RX_ERR_ARG (a size below 1, a null pointer, or a column split that
- * is not 1, 2 or 4 or leaves a share narrower than 64 columns). */
+ * Errors: RX_ERR_ARG (a size below 1 or above 2^24 (t_max, units) or 2^16
+ * (num_sms, max_splits, forced_splits), a null pointer, or a column split
+ * that is not 1, 2 or 4 or leaves a share narrower than 64 columns). */
 rx_status rx_debug_choose_partition(int t_max, int units, int D, int num_sms, int max_splits,
                                     int forced_splits, int forced_dparts, const int* cluster_capacity,
                                     int* splits, int* dparts, int* fused);

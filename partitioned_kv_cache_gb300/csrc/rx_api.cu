@@ -697,7 +697,9 @@ rx_status rx_debug_choose_partition(int t_max, int units, int D, int num_sms, in
   RX_GUARD_BEGIN
   if (!cluster_capacity || !splits || !dparts || !fused)
     return fail(RX_ERR_ARG, "rx_debug_choose_partition: null pointer");
-  if (t_max < 1 || units < 1 || num_sms < 1 || max_splits < 1 || forced_splits < 0 || forced_dparts < 0)
+  if (t_max < 1 || units < 1 || num_sms < 1 || max_splits < 1 || forced_splits < 0 || forced_dparts < 0 ||
+      t_max > (1 << 24) || units > (1 << 24) || num_sms > (1 << 16) || max_splits > (1 << 16) ||
+      forced_splits > (1 << 16))
     return fail(RX_ERR_ARG, "rx_debug_choose_partition: sizes out of range");
   if (D != 64 && D != 128 && D != 256) return fail(RX_ERR_ARG, "rx_debug_choose_partition: D = %d", D);
   rx::PartitionChoice pc;

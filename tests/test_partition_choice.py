@@ -51,6 +51,13 @@ def test_forced_values_are_kept_and_clamped(rx):
     assert choose(rx, 133, 4, max_splits=8) == (8, 2, True)     # the workspace holds 8 splits
 
 
+def test_out_of_range_sizes_are_refused(rx):
+    for kw in (dict(t_max=0, units=4), dict(t_max=34, units=0), dict(t_max=1 << 25, units=4),
+               dict(t_max=34, units=1 << 25)):
+        with pytest.raises(rx.RxError):
+            choose(rx, **kw)
+
+
 def test_invalid_column_split_is_refused(rx):
     with pytest.raises(rx.RxError):
         choose(rx, 34, 4, D=128, dparts=4)                      # 32-column shares
