@@ -20,6 +20,7 @@
 
 #include "rx.h"
 #include "rx_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -52,6 +53,23 @@ cudaError_t scratch_address(int dev, void** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Writes the state block the attention kernel reads: the window is one run of
+// W tokens (valid = W frames of one token, head 0), and the error word is
+// cleared.  The values travel as kernel arguments, so nothing on the host has
+// to outlive the call.  It waits for the stream's previous kernel, which may
+// be an earlier call still reading the block.
+__global__ void static_state_kernel(rx::DevState* st, int W) {
+  rx::grid_dependency_wait();
+  rx::grid_launch_dependents();
+  if (threadIdx.x == 0) {
+    st->head = 0;
+    st->valid = W;
+    st->pushes = 0;
+    st->append_arrivals = 0;
+    st->err = 0;
+  }
+}
 
 rx_status reject(rx_status s, const char* msg) {
   rx::set_last_error("rx_attend_regions_static", msg);
@@ -105,12 +123,10 @@ extern "C" rx_status rx_attend_regions_static(const void* q, int S, int Hq, int 
 
     // The kernel reads the window length as valid * F from the state block;
     // here the window is one run of W tokens (F = 1).  Every call rewrites the
-    // whole block, clearing the error word.
-    rx::DevState ds;
-    memset(&ds, 0, sizeof(ds));
-    ds.valid = W;
+    // block on its stream, clearing the error word.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = cudaMemcpyAsync(st, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
+    e = rx::launch_k(static_state_kernel, dim3(1), dim3(32), 0, s, st, W);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return reject(RX_ERR_CUDA, cudaGetErrorString(e));
 
     // Tensor maps over the caller's regions: (D, Hkv, tokens, 1).  An empty

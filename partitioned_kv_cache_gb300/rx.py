@@ -114,6 +114,14 @@ def _ptr(t: Optional[torch.Tensor], dtype=torch.bfloat16, name: str = "tensor",
     return t.data_ptr()
 
 
+def _shape(t: Optional[torch.Tensor], shape, name: str) -> None:
+    """Refuse a tensor whose shape differs from the one the library will
+    assume from the sizes it is given (it would read or write past the
+    caller's buffer)."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
 def launch_count() -> int:
     return int(_lib.rx_launch_count())
 
@@ -161,12 +169,21 @@ class Cache:
             pass
 
     def pin_prefix(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        c = self.cfg
         P = k.shape[1]
+        _shape(k, (c.L, P, c.Hkv, c.D), "k")
+        _shape(v, k.shape, "v")
         _check(_lib.rx_pin_prefix(self._h, _ptr(k, name="k", device=False),
                                   _ptr(v, name="v", device=False), P, _stream(stream)),
                "rx_pin_prefix")
 
+    def _frame_shape(self, k: torch.Tensor, v: torch.Tensor) -> None:
+        c = self.cfg
+        _shape(k, (c.L, c.F, c.Hkv, c.D), "k")
+        _shape(v, k.shape, "v")
+
     def push_frame(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> int:
+        self._frame_shape(k, v)
         ev = _i(0)
         _check(_lib.rx_push_frame(self._h, _ptr(k, name="k"), _ptr(v, name="v"),
                                   ctypes.byref(ev), _stream(stream)), "rx_push_frame")
@@ -176,6 +193,7 @@ class Cache:
                          consumer_stream) -> int:
         """Push on producer_stream, concurrent with attention on consumer_stream
         (needs spare_slot=1)."""
+        self._frame_shape(k, v)
         ev = _i(0)
         _check(_lib.rx_push_frame_async(self._h, _ptr(k, name="k"), _ptr(v, name="v"), ctypes.byref(ev),
                                         producer_stream.cuda_stream, consumer_stream.cuda_stream),
@@ -187,7 +205,12 @@ class Cache:
                       n_state: Optional[int] = None) -> torch.Tensor:
         """Eq. 1 for one layer; with n_state, the block-causal variant (the
         first n_state suffix tokens see only their own dynamic keys)."""
+        c = self.cfg
         S = q.shape[0]
+        _shape(q, (S, c.Hq, c.D), "q")
+        _shape(k_dyn, (S, c.Hkv, c.D), "k_dyn")
+        _shape(v_dyn, (S, c.Hkv, c.D), "v_dyn")
+        _shape(out, q.shape, "out")
         if out is None:
             out = torch.empty_like(q)
         if n_state is None:
@@ -224,15 +247,26 @@ class Cache:
                tail_len int32 CUDA tensor [B]) or None.
         Returns (out_act or None, out_lang or None).
         """
+        c = self.cfg
         S, qa, kd, vd = 0, None, None, None
         if action is not None:
             qa, kd, vd = action
             S = qa.shape[0]
+            _shape(qa, (S, c.Hq, c.D), "q")
+            _shape(kd, (S, c.Hkv, c.D), "k_dyn")
+            _shape(vd, (S, c.Hkv, c.D), "v_dyn")
+            _shape(out_act, qa.shape, "out_act")
             if out_act is None:
                 out_act = torch.empty_like(qa)
         batch = None
         if lang is not None:
             ql, kt, vt, tl = lang
+            B = ql.shape[0]
+            _shape(ql, (B, ql.shape[1] if ql.dim() > 1 else 0, c.Hq, c.D), "q_lang")
+            _shape(kt, (B, c.tail_cap, c.Hkv, c.D), "k_tail")
+            _shape(vt, kt.shape, "v_tail")
+            _shape(tl, (B,), "tail_len")
+            _shape(out_lang, ql.shape, "out_lang")
             if out_lang is None:
                 out_lang = torch.empty_like(ql)
             batch = RxStreamBatch(_ptr(ql, name="q_lang"), _ptr(kt, name="k_tail"),
@@ -295,6 +329,12 @@ def ada_gamma(t: torch.Tensor, state: torch.Tensor, W1: torch.Tensor, b1: torch.
     d = W2.shape[1]
     if cond != emb_dim + state_dim:
         raise ValueError("W1 input width %d != emb_dim + state_dim = %d" % (cond, emb_dim + state_dim))
+    _shape(t, (n_cond,), "t")
+    _shape(state, (n_cond, state_dim), "state")
+    _shape(b1, (n_sets, hidden), "b1")
+    _shape(W2, (n_sets, d, hidden), "W2")
+    _shape(b2, (n_sets, d), "b2")
+    _shape(out, (n_sets, n_cond, d), "gamma")
     if out is None:
         out = torch.empty((n_sets, n_cond, d), dtype=torch.float32, device=t.device)
     _check(_lib.rx_ada_gamma(_ptr(t, torch.float32, "t"), _ptr(state, torch.float32, "state"),
@@ -307,6 +347,8 @@ def ada_gamma(t: torch.Tensor, state: torch.Tensor, W1: torch.Tensor, b1: torch.
 def adarmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float,
                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     rows, d = x.shape
+    _shape(gamma, (d,), "gamma")
+    _shape(out, x.shape, "y")
     if out is None:
         out = torch.empty_like(x)
     _check(_lib.rx_adarmsnorm(_ptr(x, name="x"), _ptr(gamma, torch.float32, "gamma"), rows, d,
@@ -326,7 +368,15 @@ def attend_regions_static(q: torch.Tensor, k_pin: Optional[torch.Tensor], v_pin:
     """
     S, Hq, D = q.shape
     regions = [(k_pin, v_pin), (k_win, v_win), (k_dyn, v_dyn)]
-    Hkv = next((k.shape[1] for k, _ in regions if k is not None), 1)
+    for k, v in regions:
+        if (k is None) != (v is None):
+            raise ValueError("a region needs both its keys and its values (or neither)")
+    Hkv = next((k.shape[1] for k, _ in regions if k is not None and k.dim() == 3), 1)
+    for (k, v), name in zip(regions, ("pin", "win", "dyn")):
+        if k is not None:
+            _shape(k, (k.shape[0], Hkv, D), "k_" + name)
+            _shape(v, k.shape, "v_" + name)
+    _shape(out, q.shape, "out")
     counts = [0 if k is None else k.shape[0] for k, _ in regions]
     ptrs = [(_ptr(k, name="k") if n else None, _ptr(v, name="v") if n else None)
             for (k, v), n in zip(regions, counts)]
@@ -345,6 +395,13 @@ def tail_append(k_tail: torch.Tensor, v_tail: torch.Tensor, tail_len: torch.Tens
     """Append one token per (active) stream: tails [B][tail_cap][Hkv][D],
     tail_len int32 [B] (advanced on the device), new tokens [B][Hkv][D]."""
     B, tail_cap, Hkv, D = k_tail.shape
+    _shape(v_tail, k_tail.shape, "v_tail")
+    _shape(tail_len, (B,), "tail_len")
+    _shape(k_new, (B, Hkv, D), "k_new")
+    _shape(v_new, (B, Hkv, D), "v_new")
+    _shape(active, (B,), "active")
+    if overflow is not None and overflow.numel() < 1:
+        raise ValueError("overflow must hold one int32")
     _check(_lib.rx_tail_append(_ptr(k_tail, name="k_tail"), _ptr(v_tail, name="v_tail"),
                                _ptr(tail_len, torch.int32, "tail_len"), _ptr(k_new, name="k_new"),
                                _ptr(v_new, name="v_new"), _ptr(active, torch.int32, "active"), B,

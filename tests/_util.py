@@ -10,6 +10,12 @@ LIB = os.path.join(ROOT, "partitioned_kv_cache_gb300", "librx.so")
 # Attention tolerance on unit-scale inputs: max-abs 1e-2, mean-abs 1e-3.
 ATT_MAX = 1e-2
 ATT_MEAN = 1e-3
+# Fewest keys per query row for which the unit-scale bounds are held as
+# stated.  With fewer keys an output is not an average of many values: the
+# path's two bf16 roundings (P for the tensor-core product, and the output)
+# are each within 2^-9 of sum_j alpha_j |v_j| <= max|V|, so the bound for such
+# rows is 2^-8 * max|V| wherever that exceeds the unit-scale 1e-2.
+FEW_KEYS = 64
 # AdaRMSNorm: elementwise relative 1e-2, no NaN/Inf.
 NORM_REL = 1e-2
 
@@ -38,6 +44,14 @@ def check_attention(got, ref, scale=1.0):
     assert err.max() <= ATT_MAX * scale, "max abs err %.3e > %.1e" % (err.max(), ATT_MAX * scale)
     assert err.mean() <= ATT_MEAN * scale, "mean abs err %.3e > %.1e" % (err.mean(), ATT_MEAN * scale)
     return err.max(), err.mean()
+
+
+def few_keys_scale(min_keys, vmax):
+    """Widening of the attention bounds for rows that see fewer than FEW_KEYS
+    keys (1 otherwise: the stated unit-scale bounds hold)."""
+    if min_keys >= FEW_KEYS:
+        return 1.0
+    return max(1.0, 2.0 ** -8 * vmax / ATT_MAX)
 
 
 def check_norm(got, ref):

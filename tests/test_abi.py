@@ -109,3 +109,56 @@ def test_binding_checks_tensors_before_calling_the_library(lib):
         rx.adarmsnorm(x, g, 1e-6)                          # host memory
     with pytest.raises(rx.RxError):
         rx.choose_partition(34, 4, 96, 152, 64, [0] * 17)  # head dimension 96
+
+
+def test_binding_refuses_shapes_the_library_would_overrun(lib):
+    """Sizes passed to the library come from the tensors' shapes; a tensor of
+    another shape (a shorter V, a smaller output, another head count) is
+    refused in Python before any C call, so the kernels never read or write
+    past a caller's buffer (CPU only: host tensors, no cache handle)."""
+    import torch
+    from partitioned_kv_cache_gb300 import rx
+    bf = dict(dtype=torch.bfloat16)
+    q = torch.zeros(5, 8, 64, **bf)
+    k = torch.zeros(7, 1, 64, **bf)
+    out = torch.zeros(5, 8, 64, **bf)
+    static = rx.attend_regions_static
+    with pytest.raises(ValueError, match="v_pin"):
+        static(q, k, k[:6], None, None, None, None, out)                 # shorter V
+    with pytest.raises(ValueError, match="k_win"):
+        static(q, k, k, torch.zeros(7, 2, 64, **bf), torch.zeros(7, 2, 64, **bf), None, None, out)
+    with pytest.raises(ValueError, match="k_dyn"):
+        static(q, None, None, None, None, torch.zeros(3, 1, 128, **bf), torch.zeros(3, 1, 128, **bf), out)
+    with pytest.raises(ValueError, match="out"):
+        static(q, k, k, None, None, None, None, out[:4])                  # smaller output
+    with pytest.raises(ValueError, match="both"):
+        static(q, k, None, None, None, None, None, out)
+    with pytest.raises(ValueError, match="gamma"):
+        rx.adarmsnorm(torch.zeros(4, 64, **bf), torch.ones(32), 1e-6)
+    with pytest.raises(ValueError, match="y"):
+        rx.adarmsnorm(torch.zeros(4, 64, **bf), torch.ones(64), 1e-6, out=torch.zeros(3, 64, **bf))
+    with pytest.raises(ValueError, match="v_new"):
+        rx.tail_append(torch.zeros(2, 4, 1, 64, **bf), torch.zeros(2, 4, 1, 64, **bf),
+                       torch.zeros(2, dtype=torch.int32), torch.zeros(2, 1, 64, **bf),
+                       torch.zeros(1, 1, 64, **bf))
+    W1 = torch.zeros(2, 64, 32, **bf)
+    with pytest.raises(ValueError, match="W2"):
+        rx.ada_gamma(torch.zeros(3), torch.zeros(3, 16), W1, torch.zeros(2, 64, **bf),
+                     torch.zeros(2, 128, 32, **bf), torch.zeros(2, 128, **bf), 16)
+    # The cache's calls check against its configuration (no device needed).
+    c = rx.Cache.__new__(rx.Cache)
+    c.cfg = rx.RxConfig(2, 8, 1, 64, 16, 4, 32, 51, 8, 4, 0)
+    c._h = None
+    with pytest.raises(ValueError, match="k_dyn"):
+        c.attend_suffix(0, torch.zeros(5, 8, 64, **bf), torch.zeros(4, 1, 64, **bf), torch.zeros(5, 1, 64, **bf))
+    with pytest.raises(ValueError, match="q"):
+        c.attend_suffix(0, torch.zeros(5, 4, 64, **bf), torch.zeros(5, 1, 64, **bf), torch.zeros(5, 1, 64, **bf))
+    with pytest.raises(ValueError, match="out"):
+        c.attend_suffix(0, q, q[:, :1].contiguous(), q[:, :1].contiguous(), out=out[:, :4].contiguous())
+    with pytest.raises(ValueError, match="k"):
+        c.push_frame(torch.zeros(2, 31, 1, 64, **bf), torch.zeros(2, 31, 1, 64, **bf))
+    with pytest.raises(ValueError, match="v"):
+        c.pin_prefix(torch.zeros(2, 16, 1, 64, **bf), torch.zeros(2, 15, 1, 64, **bf))
+    with pytest.raises(ValueError, match="k_tail"):
+        c.attend_batch(0, None, (torch.zeros(4, 1, 8, 64, **bf), torch.zeros(4, 7, 1, 64, **bf),
+                                 torch.zeros(4, 7, 1, 64, **bf), torch.zeros(4, dtype=torch.int32)))
