@@ -11,7 +11,7 @@ captured once as a CUDA graph and replayed.  value = denoise steps per second
 (ticks x K / time).  Inputs are seeded synthetic tensors already resident in
 HBM; two input pools larger than L2 alternate between ticks.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c4]
     python bench.py --impl reference ...   # the CPU fp64 oracle, timed on host cores
 
 Under torchrun (N > 1) every rank runs an independent replica (the method has
@@ -40,9 +40,10 @@ UNIT = "denoise-steps/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
-# launch from the ncu capture summarised in profiles/attn_kernel_c3.md.  It is
-# reported only while the kernel's code (its source file and the two headers it
-# includes, comments and blank lines removed) still matches the code captured.
+# call (its kernels' launches) from an ncu capture of the same workload.  It is
+# reported only while the kernel's code (its source file and the headers it
+# includes, comments and blank lines removed) still matches the code captured;
+# otherwise the line carries null.
 ATTN_TRAFFIC = {"sha256_16": "42569ab315170198", "workload": "c3", "bytes": 2.498e6}
 ATTN_SOURCES = ("partitioned_attn.cu", "partition.h", "rx_internal.h", "sm103_ptx.cuh")
 
@@ -278,6 +279,56 @@ def max_over_ranks(ms: float, world: int, device) -> float:
 def replica_throughput(units_per_rank: int, world: int, ms: float) -> float:
     """Whole-job units per second: every rank processed units_per_rank."""
     return units_per_rank * world / (ms / 1e3)
+
+
+def attention_call_us(rx, wl, stream, randn_bf16, reps=3):
+    """Per-call time of the workload's attention (every layer, every step of a
+    tick, one CUDA graph) on a store with a full window; (us, FLOP per call)."""
+    import torch
+    L, S, Hq, Hkv, D, K, B = wl.L, wl.S, wl.Hq, wl.Hkv, wl.D, wl.steps, wl.n_lang
+    cache = rx.Cache(L, Hq, Hkv, D, wl.P, wl.N, wl.F, S, wl.tail_cap, B)
+    cache.pin_prefix(randn_bf16(L, wl.P, Hkv, D), randn_bf16(L, wl.P, Hkv, D))
+    q = randn_bf16(K, L, S, Hq, D)
+    kd = randn_bf16(K, L, S, Hkv, D)
+    vd = randn_bf16(K, L, S, Hkv, D)
+    o = torch.empty_like(q)
+    if B:
+        ql = randn_bf16(K, L, B, 1, Hq, D)
+        ol = torch.empty_like(ql)
+        tails_k = randn_bf16(L, B, wl.tail_cap, Hkv, D)
+        tails_v = randn_bf16(L, B, wl.tail_cap, Hkv, D)
+        tail_len = torch.randint(0, wl.tail_max + 1, (L, B), device=q.device, dtype=torch.int32)
+
+    def calls():
+        for k in range(K):
+            for l in range(L):
+                if B:
+                    cache.attend_batch(l, (q[k, l], kd[k, l], vd[k, l]),
+                                       (ql[k, l], tails_k[l], tails_v[l], tail_len[l]),
+                                       out_act=o[k, l], out_lang=ol[k, l])
+                else:
+                    cache.attend_suffix(l, q[k, l], kd[k, l], vd[k, l], out=o[k, l])
+
+    with torch.cuda.stream(stream):
+        for t in range(wl.N):
+            cache.push_frame(randn_bf16(L, wl.F, Hkv, D), randn_bf16(L, wl.F, Hkv, D))
+        calls()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        calls()
+    with torch.cuda.stream(stream):
+        gr.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+    e1.synchronize()
+    assert cache.check_device_error() == 0, "a kernel reported a device-side timeout"
+    cache.close()
+    return e0.elapsed_time(e1) * 1e3 / (reps * K * L), attn_flops(wl)
 
 
 def run_ours(args, wl):
@@ -550,55 +601,85 @@ def run_ours(args, wl):
     del qb, kb, vb, ob, bg
 
     # ---------------- end to end through the API with host buffers ----------------
-    h_fk = torch.empty((L, wl.F, Hkv, D), dtype=torch.bfloat16).pin_memory()
-    h_fv = torch.empty_like(h_fk).pin_memory()
-    h_fk.copy_(frames[0][0].cpu())
-    h_fv.copy_(frames[0][1].cpu())
-    h_x = x[0, 0, 0, 0].cpu().pin_memory()
-    h_state = state[0].cpu().pin_memory()
-    h_out = torch.empty((S, Hq, D), dtype=torch.bfloat16).pin_memory()
+    # Every tick moves all of its inputs from pinned host memory (the frame's
+    # K/V, the robot state, and every step's and layer's q, k_dyn, v_dyn and
+    # norm inputs) and reads all of its outputs back (every attention output
+    # and both norms' outputs).  The next tick's inputs upload on a copy
+    # stream into the other input slot while this tick computes, and this
+    # tick's outputs download on a second copy stream while the next one
+    # computes, as a streaming deployment would overlap them.  A slot's
+    # upload waits for the tick that last read it, and a tick waits for the
+    # download of the outputs it is about to overwrite.  Every copy is inside
+    # the timed region.
+    ins = [lambda s_: frames[s_][0], lambda s_: frames[s_][1], lambda s_: state[s_],
+           lambda s_: q[s_], lambda s_: kd[s_], lambda s_: vd[s_], lambda s_: x[s_]]
+    outs = [lambda s_: o[s_], lambda s_: y[s_]]
+    if B:
+        ins.append(lambda s_: ql[s_])
+        outs.append(lambda s_: ol[s_])
+    h_in = [fn(0).cpu().pin_memory() for fn in ins]
+    h_out = [torch.empty(fn(0).shape, dtype=fn(0).dtype).pin_memory() for fn in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
     e2e_steps = max(4, args.steps // 4)
-    h2d = (h_fk.numel() + h_fv.numel() + h_x.numel()) * 2 + h_state.numel() * 4
-    d2h = h_out.numel() * 2
-    # The next tick's inputs upload on a copy stream into the other input slot
-    # while this tick computes (the slots alternate, so an upload waits only
-    # for the tick that last read its slot); each tick's result is read back
-    # on the compute stream right after its graph.
-    copy_stream = torch.cuda.Stream(device=dev)
-    ready = [torch.cuda.Event() for _ in range(NSLOT)]
-    free = [torch.cuda.Event() for _ in range(NSLOT)]
+    up_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(NSLOT)]      # slot's inputs uploaded
+    consumed = [torch.cuda.Event() for _ in range(NSLOT)]   # slot's tick finished
+    drained = [torch.cuda.Event() for _ in range(NSLOT)]    # slot's outputs downloaded
 
-    def upload(s):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(free[s])
-            frames[s][0].copy_(h_fk, non_blocking=True)
-            frames[s][1].copy_(h_fv, non_blocking=True)
-            x[s, 0, 0, 0].copy_(h_x, non_blocking=True)
-            state[s].copy_(h_state, non_blocking=True)
-            ready[s].record(copy_stream)
+    def upload(s_):
+        with torch.cuda.stream(up_stream):
+            up_stream.wait_event(consumed[s_])
+            for fn, h in zip(ins, h_in):
+                fn(s_).copy_(h, non_blocking=True)
+            ready[s_].record(up_stream)
+
+    def download(s_):
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(consumed[s_])
+            for fn, h in zip(outs, h_out):
+                h.copy_(fn(s_), non_blocking=True)
+            drained[s_].record(down_stream)
 
     with torch.cuda.stream(stream):
-        for s in range(NSLOT):
-            free[s].record(stream)
+        for s_ in range(NSLOT):
+            consumed[s_].record(stream)
+            drained[s_].record(stream)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        copy_stream.wait_stream(stream)   # every upload is inside the timed region
+        up_stream.wait_stream(stream)     # every copy is inside the timed region
+        down_stream.wait_stream(stream)
         upload(0)
         for i in range(e2e_steps):
-            s = i % NSLOT
+            s_ = i % NSLOT
             if i + 1 < e2e_steps:
                 upload((i + 1) % NSLOT)
-            stream.wait_event(ready[s])
-            graphs[s].replay()
-            free[s].record(stream)
-            h_out.copy_(o[s, K - 1, L - 1], non_blocking=True)
+            stream.wait_event(ready[s_])
+            stream.wait_event(drained[s_])
+            graphs[s_].replay()
+            consumed[s_].record(stream)
+            download(s_)
+        stream.wait_stream(down_stream)
         f1.record(stream)
     f1.synchronize()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     e2e_val = replica_throughput(e2e_steps * K, world, e2e_ms)
     assert cache.check_device_error() == 0, "a kernel reported a device-side timeout"
+    del h_in, h_out
+
+    # ---------------- the other multi-layer workloads' attention calls ----------------
+    for other in ("c3", "c4", "c5"):
+        if other == args.workload:
+            continue
+        us, flo = attention_call_us(rx, W.WORKLOADS[other], stream, randn_bf16, reps=3)
+        kern["attention_" + other] = {
+            "us_per_call": us, "flops_per_call": flo, "TFLOP/s": flo / us / 1e6,
+            "frac_tensor": flo / us / 1e6 / peak_tf,
+            "note": "%s, graph of %d x %d calls over one input set" % (
+                describe(W.WORKLOADS[other]), W.WORKLOADS[other].steps, W.WORKLOADS[other].L)}
 
     if rank != 0:
         return
@@ -622,6 +703,9 @@ def run_ours(args, wl):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": attn_traffic(args.workload),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one call "
+                                       "from a capture of this workload, reported only while the kernel "
+                                       "code hash matches that capture (else null)",
                      "kernel": "partitioned attention (split-KV kernel + merge), %.2f us per call, "
                                "%.3g algorithmic FLOP per call (4*Hq*S*Lk*D)" % (attn_us, fl),
                      "peak_kind": "%s bf16 dense burst" % peak_kind},
@@ -642,7 +726,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="c3", choices=["c2", "c3", "c4", "c5"])
+    ap.add_argument("--workload", default="c4", choices=["c2", "c3", "c4", "c5"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--splits", type=int, default=0, help="split-KV partitions (0 = automatic)")

@@ -131,9 +131,13 @@ def test_batch_argument_errors(rx):
     cache, _ = _setup(rx, wl, 35, 1)
     lq, ltk, ltv, lln, lang = _lang(wl, 35, 0, 0, 0)
     big = torch.zeros((17, 1, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(rx.RxError) as e:
-        cache.attend_batch(0, None, (big, lang[1], lang[2], lang[3]))
+    big_tail = torch.zeros((17, wl.tail_cap, wl.Hkv, wl.D), dtype=torch.bfloat16, device="cuda")
+    big_len = torch.zeros(17, dtype=torch.int32, device="cuda")
+    with pytest.raises(rx.RxError) as e:      # 17 query tokens > max_req = 16
+        cache.attend_batch(0, None, (big, big_tail, big_tail, big_len))
     assert e.value.status == -3
+    with pytest.raises(ValueError):           # tails of 16 streams for 17 queries
+        cache.attend_batch(0, None, (big, lang[1], lang[2], lang[3]))
     with pytest.raises(rx.RxError) as e:
         cache.attend_batch(wl.L, None, lang)
     assert e.value.status == -2

@@ -65,6 +65,7 @@ def test_push_rejects_misaligned_frames(rx):
     import torch
     cache = rx.Cache(1, 2, 1, 64, 16, 2, 16, 8)
     k = torch.zeros(16 * 64 + 1, dtype=torch.bfloat16, device="cuda")
+    km = k[1:].view(1, 16, 1, 64)    # the right shape, 2 bytes off a 16-byte boundary
     with pytest.raises(rx.RxError):
-        cache.push_frame(k[1:], k[1:])
+        cache.push_frame(km, km)
     cache.close()

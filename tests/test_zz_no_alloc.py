@@ -65,10 +65,11 @@ def test_static_entry_matches_the_oracle_on_two_calls(case):
     results = []
     for host, tens in calls:
         rx.attend_regions_static(*tens, out)
-        results.append(host64(out))
+        results.append(out.cpu())     # bf16 straight to the host: no device allocation here
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free0, "the static entry point changed free device memory"
-    for (host, _), got in zip(calls, results):
+    for (host, _), res in zip(calls, results):
+        got = host64(res)
         q, kp, vp, kw, vw, kd, vd = (f(a) for a in host)
         ref = OA.partitioned_attention(q, [kp, kw, kd], [vp, vw, vd])
         vmax = max(float(np.abs(v).max()) for v in (vp, vw, vd) if v.size)
