@@ -188,6 +188,46 @@ rx_status rx_attend_batch(rx_cache_t cache, int layer, const void* q_act,
                           void* out_act, const rx_stream_batch* lang,
                           void* stream);
 
+/* One AdaRMSNorm ("Reflex ...", §III Eq. (2); §V forward) over `rows` rows
+ * of width d, for an attention call to run in the same launch:
+ *   y = x * rsqrt(mean(x^2) + eps) * gamma, mean of squares in fp32.
+ * x, y: bf16 [rows][d] device memory; gamma: fp32 [d]; d % 8 == 0; rows >= 0;
+ * all 16-byte aligned.  y may not overlap x or another job's x or y. */
+typedef struct rx_norm_rows {
+  const void* x;
+  const float* gamma;
+  void* y;
+  int rows;
+  int d;
+  float eps;
+} rx_norm_rows;
+#define RX_MAX_NORM_JOBS 2
+
+/* rx_attend_suffix and up to RX_MAX_NORM_JOBS AdaRMSNorm jobs in ONE launch,
+ * the FP32-variance AdaRMSNorm fused in beside the partitioned attention
+ * ("Reflex ...", §III "Model components": AdaRMSNorm before the attention and
+ * before the MLP of every layer).  The attention output
+ * is that of rx_attend_suffix and every y is bit for bit that of
+ * rx_adarmsnorm on the same arguments.  The norm rows run on the attention
+ * CTAs' softmax warps while those wait for their first score tile.  The jobs
+ * must not read what the attention call writes or write what it reads (the
+ * launch runs both at once).  n_norms = 0 is rx_attend_suffix.
+ * Errors: those of rx_attend_suffix and rx_adarmsnorm (RX_ERR_ARG for a bad
+ * job). */
+rx_status rx_attend_suffix_norms(rx_cache_t cache, int layer, const void* q,
+                                 const void* k_dyn, const void* v_dyn, int S,
+                                 void* out, const rx_norm_rows* norms,
+                                 int n_norms, void* stream);
+
+/* rx_attend_batch with norm jobs in the same launch, as
+ * rx_attend_suffix_norms.  With neither an action suffix nor language
+ * streams, the jobs run as rx_adarmsnorm launches. */
+rx_status rx_attend_batch_norms(rx_cache_t cache, int layer, const void* q_act,
+                                const void* k_dyn, const void* v_dyn, int S,
+                                void* out_act, const rx_stream_batch* lang,
+                                const rx_norm_rows* norms, int n_norms,
+                                void* stream);
+
 /* Append one token to each active language stream's private tail (cross-frame
  * continuous batching, "OxyGen ...", §"Core method": a stream's KV cache grows
  * by one entry per decoded token and the stream resumes across frames).

@@ -20,6 +20,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "norm_row.cuh"
 #include "rx_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -35,11 +36,6 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   }
 }
 
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // SM count of device `dev`, queried once per device.
 cudaError_t device_sm_count(int dev, int* out) {
   static std::atomic<int> cache[64];
@@ -50,14 +46,9 @@ cudaError_t device_sm_count(int dev, int* out) {
   return e;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// One warp per row.  MAXV = 16-byte vectors per lane kept in registers
-// (d <= 256 * MAXV); MAXV = 0 selects the two-pass path for wider rows.
+// One warp per row (adarmsnorm_row).  MAXV = 16-byte vectors per lane kept
+// in registers (d <= 256 * MAXV); MAXV = 0 selects the two-pass path for
+// wider rows.
 template <int MAXV>
 __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict__ x,
                                                          const float* __restrict__ gamma,
@@ -78,66 +69,7 @@ __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict
   grid_dependency_wait();
   grid_launch_dependents();
   if (row >= rows) return;
-  const uint4* xr = x + row * nv;
-  uint4* yr = y + row * nv;
-  const float inv_d = 1.0f / static_cast<float>(d);
-  if constexpr (MAXV > 0) {
-    // The row and its gamma slice are loaded together, so the gamma read is
-    // not a second round trip after the reduction.
-    uint4 xv[MAXV];
-    float4 g0[MAXV], g1[MAXV];
-#pragma unroll
-    for (int u = 0; u < MAXV; ++u) {
-      const int v = lane + 32 * u;
-      if (v < nv) {
-        xv[u] = xr[v];
-        g0[u] = *reinterpret_cast<const float4*>(gamma + 8 * v);
-        g1[u] = *reinterpret_cast<const float4*>(gamma + 8 * v + 4);
-      }
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int u = 0; u < MAXV; ++u) {
-      if (lane + 32 * u < nv) {
-        float f[8];
-        unpack8(xv[u], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-      }
-    }
-    const float r = rsqrtf(warp_sum(ss) * inv_d + eps);
-#pragma unroll
-    for (int u = 0; u < MAXV; ++u) {
-      const int v = lane + 32 * u;
-      if (v < nv) {
-        float f[8];
-        unpack8(xv[u], f);
-        yr[v] = make_uint4(pack2(f[0] * r * g0[u].x, f[1] * r * g0[u].y),
-                           pack2(f[2] * r * g0[u].z, f[3] * r * g0[u].w),
-                           pack2(f[4] * r * g1[u].x, f[5] * r * g1[u].y),
-                           pack2(f[6] * r * g1[u].z, f[7] * r * g1[u].w));
-      }
-    }
-  } else {
-    float ss = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-      float f[8];
-      unpack8(xr[v], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-    }
-    const float r = rsqrtf(warp_sum(ss) * inv_d + eps);
-    for (int v = lane; v < nv; v += 32) {
-      float f[8];
-      unpack8(xr[v], f);
-      const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * v);
-      const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * v + 4);
-      yr[v] = make_uint4(pack2(f[0] * r * g0.x, f[1] * r * g0.y),
-                         pack2(f[2] * r * g0.z, f[3] * r * g0.w),
-                         pack2(f[4] * r * g1.x, f[5] * r * g1.y),
-                         pack2(f[6] * r * g1.z, f[7] * r * g1.w));
-    }
-  }
+  adarmsnorm_row<MAXV>(x + row * nv, gamma, nv, 1.0f / static_cast<float>(d), eps, y + row * nv, lane);
 }
 
 // ---------------------------------------------------------------- gamma MLP

@@ -55,6 +55,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "norm_row.cuh"
 #include "partition.h"
 #include "rx_internal.h"
 #include "sm103_ptx.cuh"
@@ -126,8 +127,21 @@ struct SegParams {
   int state_tokens;      // block-causal: tokens below see private keys [0, state_tokens) only
 };
 
+// An AdaRMSNorm job run by the launch's softmax warps (NormJob, device form).
+struct NormParams {
+  const uint4* x;
+  const float* gamma;
+  uint4* y;
+  int rows;
+  int nv;        // 16-byte vectors per row (d / 8)
+  float inv_d;
+  float eps;
+};
+
 struct AttnParams {
   SegParams seg[2];
+  NormParams norm[kMaxNormJobs];
+  int n_norm_rows;       // rows of all norm jobs (0: none)
   CUtensorMap tm_k[2];   // pin, window when not pre-tiled: (D, Hkv, keys, layers), box (64, 1, 64, 1)
   CUtensorMap tm_v[2];
   const uint8_t* k_tiles[2];   // pre-tiled pin / window of (layer, head 0); null = tensor map
@@ -295,6 +309,32 @@ __device__ __forceinline__ void cluster_combine(const uint4* xo, const float2* x
   }
 }
 
+// Norm rows of the launch's jobs, in job order, are shared out over the
+// grid's CTAs and, within a CTA, over its four softmax warps: row r goes to
+// CTA r mod nCTA, warp (r / nCTA) mod 4.  (The warp's first row: r = cta +
+// nCTA * sw.)
+__device__ __forceinline__ int first_norm_row(int sw) {
+  const int ncta = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+  const int cta = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  return cta + ncta * sw;
+}
+
+// The norm rows of softmax warp sw (0..3) of this CTA.  They run after the
+// dependency wait, while the warp would otherwise wait for its first score
+// tile (the producer has issued Q and the first key tile by then).
+__device__ __noinline__ void run_norm_rows(const AttnParams& p, int sw, int lane) {
+  const int ncta = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+  for (int r = first_norm_row(sw); r < p.n_norm_rows; r += 4 * ncta) {
+    const int j = r < p.norm[0].rows ? 0 : 1;
+    const NormParams& nj = p.norm[j];
+    const size_t row = static_cast<size_t>(j ? r - p.norm[0].rows : r);
+    if (nj.nv <= 128)
+      adarmsnorm_row<4>(nj.x + row * nj.nv, nj.gamma, nj.nv, nj.inv_d, nj.eps, nj.y + row * nj.nv, lane);
+    else
+      adarmsnorm_row<0>(nj.x + row * nj.nv, nj.gamma, nj.nv, nj.inv_d, nj.eps, nj.y + row * nj.nv, lane);
+  }
+}
+
 // CM: the most splits a launch of this build may merge in a cluster
 // (kMaxClusterSplits, or a small count whose combine keeps several rows'
 // loads in flight per thread), or kMergeWide: up to kMaxClusterSplits splits
@@ -357,6 +397,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (sg.n_priv > 0) {
       tma_prefetch_desc(&sg.tm_kp);
       tma_prefetch_desc(&sg.tm_vp);
+    }
+  }
+  // Norm rows of this CTA's softmax warps: fetch the first row and its gamma
+  // into L2 while the previous kernel drains (a hint, safe before the wait).
+  if (p.n_norm_rows > 0 && warp >= 2 && warp <= 5 && lane == 0) {
+    const int r = first_norm_row(warp - 2);
+    if (r < p.n_norm_rows) {
+      const int j = r < p.norm[0].rows ? 0 : 1;
+      const NormParams& nj = p.norm[j];
+      const size_t row = static_cast<size_t>(j ? r - p.norm[0].rows : r);
+      bulk_prefetch_l2(nj.x + row * nj.nv, static_cast<uint32_t>(nj.nv) * 16u);
+      bulk_prefetch_l2(nj.gamma, static_cast<uint32_t>(nj.nv) * 32u);
     }
   }
   tc_fence_before();
@@ -570,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
     if (sg.state_tokens > 0 && Rs / p.G < sg.state_tokens) hi = min(hi, sg.state_tokens);
     const bool priv_masked = sg.tail_cap > 0 || sg.state_tokens > 0;
+    if (p.n_norm_rows > 0 && warp <= 5) run_norm_rows(p, warp - 2, lane);
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = n > 0;
@@ -1059,6 +1112,19 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
     t_max = t > t_max ? t : t_max;
   }
   if (nseg == 1) prm.seg[1].row_base = m_total * kBM;   // no second segment
+  if (a.n_norms < 0 || a.n_norms > kMaxNormJobs) return cudaErrorInvalidValue;
+  for (int i = 0; i < a.n_norms; ++i) {
+    const NormJob& nj = a.norms[i];
+    NormParams& np = prm.norm[i];
+    np.x = static_cast<const uint4*>(nj.x);
+    np.gamma = nj.gamma;
+    np.y = static_cast<uint4*>(nj.y);
+    np.rows = nj.rows;
+    np.nv = nj.d / 8;
+    np.inv_d = 1.0f / static_cast<float>(nj.d);
+    np.eps = nj.eps;
+    prm.n_norm_rows += nj.rows;
+  }
   if (!a.pin_k_tiles) {
     prm.tm_k[0] = *a.tm_pin_k;
     prm.tm_v[0] = *a.tm_pin_v;

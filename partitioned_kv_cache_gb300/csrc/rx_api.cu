@@ -380,6 +380,80 @@ static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   return a;
 }
 
+// Checks the norm jobs an attention launch runs beside its key loop and
+// copies them into `jobs`.  The same conditions as rx_adarmsnorm, plus: no
+// job's output may overlap another job's input or output.
+static rx_status check_norms(const char* where, const rx_norm_rows* norms, int n_norms,
+                             rx::NormJob* jobs) {
+  if (n_norms < 0 || n_norms > RX_MAX_NORM_JOBS)
+    return fail(RX_ERR_ARG, "%s: n_norms = %d not in [0, %d]", where, n_norms, RX_MAX_NORM_JOBS);
+  if (n_norms > 0 && !norms) return fail(RX_ERR_ARG, "%s: null norm jobs", where);
+  long long total = 0;
+  for (int i = 0; i < n_norms; ++i) {
+    const rx_norm_rows& n = norms[i];
+    if (n.rows < 0) return fail(RX_ERR_ARG, "%s: norm job %d: rows < 0", where, i);
+    if (n.d < 8 || (n.d & 7)) return fail(RX_ERR_ARG, "%s: norm job %d: d = %d must be a positive multiple of 8", where, i, n.d);
+    if (!(n.eps >= 0.f)) return fail(RX_ERR_ARG, "%s: norm job %d: eps must be >= 0", where, i);
+    if (n.rows > 0) {
+      if (!n.x || !n.gamma || !n.y) return fail(RX_ERR_ARG, "%s: norm job %d: null pointer", where, i);
+      if (!aligned16(n.x) || !aligned16(n.y) || !aligned16(n.gamma))
+        return fail(RX_ERR_ARG, "%s: norm job %d: pointers must be 16-byte aligned", where, i);
+    }
+    total += n.rows;
+    jobs[i] = rx::NormJob{n.x, n.gamma, n.y, n.rows, n.d, n.eps};
+  }
+  if (total > (1LL << 30)) return fail(RX_ERR_ARG, "%s: too many norm rows", where);
+  // y of every job against x and y of every job (byte ranges).
+  for (int i = 0; i < n_norms; ++i) {
+    if (jobs[i].rows == 0) continue;
+    const char* y0 = static_cast<const char*>(jobs[i].y);
+    const char* y1 = y0 + static_cast<size_t>(jobs[i].rows) * jobs[i].d * 2;
+    for (int j = 0; j < n_norms; ++j) {
+      if (jobs[j].rows == 0) continue;
+      const size_t b = static_cast<size_t>(jobs[j].rows) * jobs[j].d * 2;
+      const char* x0 = static_cast<const char*>(jobs[j].x);
+      if (y0 < x0 + b && x0 < y1) return fail(RX_ERR_ARG, "%s: norm job %d's y overlaps job %d's x", where, i, j);
+      const char* z0 = static_cast<const char*>(jobs[j].y);
+      if (j != i && y0 < z0 + b && z0 < y1)
+        return fail(RX_ERR_ARG, "%s: norm jobs %d and %d write overlapping rows", where, i, j);
+    }
+  }
+  return RX_OK;
+}
+
+static rx_status attend_suffix_impl(const char* where, rx_cache_t h, int layer, const void* q,
+                                    const void* k_dyn, const void* v_dyn, int S, void* out,
+                                    const rx_norm_rows* norms, int n_norms, void* stream) {
+  if (!h) return fail(RX_ERR_ARG, "%s: null cache", where);
+  const rx_config& c = h->cfg;
+  if (layer < 0 || layer >= c.L) return fail(RX_ERR_LAYER, "%s: layer %d not in [0, %d)", where, layer, c.L);
+  if (S < 1) return fail(RX_ERR_ARG, "%s: S < 1", where);
+  if (S > c.S_cap) return fail(RX_ERR_CAPACITY, "%s: S = %d > S_cap = %d", where, S, c.S_cap);
+  if (!q || !k_dyn || !v_dyn || !out) return fail(RX_ERR_ARG, "%s: null pointer", where);
+  if (!aligned16(q) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out))
+    return fail(RX_ERR_ARG, "%s: pointers must be 16-byte aligned", where);
+  rx::NormJob jobs[rx::kMaxNormJobs];
+  const rx_status ns = check_norms(where, norms, n_norms, jobs);
+  if (ns != RX_OK) return ns;
+  rx::AttnLaunch a = make_launch(h, layer);
+  a.norms = jobs;
+  a.n_norms = n_norms;
+  rx::AttnSegment seg{q, k_dyn, v_dyn, out, S, S, nullptr, 1, 0, 0};
+  cudaError_t e = rx::launch_partitioned_attention(a, &seg, 1, static_cast<cudaStream_t>(stream), nullptr);
+  if (e != cudaSuccess)
+    return fail(RX_ERR_CUDA, "%s: launch: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return RX_OK;
+}
+
+rx_status rx_attend_suffix_norms(rx_cache_t h, int layer, const void* q, const void* k_dyn,
+                                 const void* v_dyn, int S, void* out, const rx_norm_rows* norms,
+                                 int n_norms, void* stream) {
+  RX_GUARD_BEGIN
+  return attend_suffix_impl("rx_attend_suffix_norms", h, layer, q, k_dyn, v_dyn, S, out, norms, n_norms,
+                            stream);
+  RX_GUARD_END
+}
+
 rx_status rx_attend_suffix(rx_cache_t h, int layer, const void* q, const void* k_dyn,
                            const void* v_dyn, int S, void* out, void* stream) {
   RX_GUARD_BEGIN
@@ -511,10 +585,29 @@ rx_status rx_restore(rx_cache_t h, const void* src, void* stream) {
   RX_GUARD_END
 }
 
+static rx_status attend_batch_impl(rx_cache_t h, int layer, const void* q_act, const void* k_dyn,
+                                   const void* v_dyn, int S, void* out_act, const rx_stream_batch* lang,
+                                   const rx_norm_rows* norms, int n_norms, void* stream);
+
 rx_status rx_attend_batch(rx_cache_t h, int layer, const void* q_act, const void* k_dyn,
                           const void* v_dyn, int S, void* out_act, const rx_stream_batch* lang,
                           void* stream) {
   RX_GUARD_BEGIN
+  return attend_batch_impl(h, layer, q_act, k_dyn, v_dyn, S, out_act, lang, nullptr, 0, stream);
+  RX_GUARD_END
+}
+
+rx_status rx_attend_batch_norms(rx_cache_t h, int layer, const void* q_act, const void* k_dyn,
+                                const void* v_dyn, int S, void* out_act, const rx_stream_batch* lang,
+                                const rx_norm_rows* norms, int n_norms, void* stream) {
+  RX_GUARD_BEGIN
+  return attend_batch_impl(h, layer, q_act, k_dyn, v_dyn, S, out_act, lang, norms, n_norms, stream);
+  RX_GUARD_END
+}
+
+static rx_status attend_batch_impl(rx_cache_t h, int layer, const void* q_act, const void* k_dyn,
+                                   const void* v_dyn, int S, void* out_act, const rx_stream_batch* lang,
+                                   const rx_norm_rows* norms, int n_norms, void* stream) {
   if (!h) return fail(RX_ERR_ARG, "rx_attend_batch: null cache");
   const rx_config& c = h->cfg;
   if (layer < 0 || layer >= c.L) return fail(RX_ERR_LAYER, "rx_attend_batch: layer %d not in [0, %d)", layer, c.L);
@@ -543,12 +636,29 @@ rx_status rx_attend_batch(rx_cache_t h, int layer, const void* q_act, const void
     segs[nseg++] = rx::AttnSegment{b.q, b.k_tail, b.v_tail, b.out, b.B * b.T, b.B * c.tail_cap,
                                    b.tail_len, b.T, c.tail_cap, 0};
   }
-  if (nseg == 0) return RX_OK;
-  const rx::AttnLaunch a = make_launch(h, layer);
+  rx::NormJob jobs[rx::kMaxNormJobs];
+  const rx_status ns = check_norms("rx_attend_batch", norms, n_norms, jobs);
+  if (ns != RX_OK) return ns;
+  int norm_rows = 0;
+  for (int i = 0; i < n_norms; ++i) norm_rows += jobs[i].rows;
+  if (nseg == 0) {
+    // No attention: the norm jobs alone, as rx_adarmsnorm launches.
+    for (int i = 0; i < n_norms; ++i) {
+      if (jobs[i].rows == 0) continue;
+      const cudaError_t e = rx::launch_adarmsnorm(static_cast<const __nv_bfloat16*>(jobs[i].x), jobs[i].gamma,
+                                                  jobs[i].rows, jobs[i].d, jobs[i].eps,
+                                                  static_cast<__nv_bfloat16*>(jobs[i].y),
+                                                  static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e, "rx_attend_batch: norm launch");
+    }
+    return RX_OK;
+  }
+  rx::AttnLaunch a = make_launch(h, layer);
+  a.norms = jobs;
+  a.n_norms = norm_rows > 0 ? n_norms : 0;
   cudaError_t e = rx::launch_partitioned_attention(a, segs, nseg, static_cast<cudaStream_t>(stream), nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "rx_attend_batch: launch");
   return RX_OK;
-  RX_GUARD_END
 }
 
 rx_status rx_ada_gamma(const float* t, const float* state, int n_cond, int emb_dim, int state_dim,

@@ -114,6 +114,18 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
 constexpr int kBM = 128;   // query rows per CTA (one tcgen05 M=128 tile)
 constexpr int kBN = 64;    // keys per KV tile
 
+// An AdaRMSNorm job (y = x * rsqrt(mean x^2 + eps) * gamma over `rows` rows
+// of width d) that an attention launch runs beside its key loop.
+struct NormJob {
+  const void* x;        // bf16 [rows][d]
+  const float* gamma;   // fp32 [d]
+  void* y;              // bf16 [rows][d]
+  int rows;
+  int d;                // multiple of 8
+  float eps;
+};
+constexpr int kMaxNormJobs = 2;
+
 struct AttnLaunch {
   // Shared regions (pinned, window) of one layer.  Each is either pre-tiled
   // (pointers below non-null: bulk copies) or read through its tensor map.
@@ -138,6 +150,8 @@ struct AttnLaunch {
   int forced_dparts;  // output-column split: 0 = automatic, else 1, 2 or 4
   int num_sms;
   int inject_tx;      // test aid: extra bytes CTA 0 expects on its first K tile (0 = none)
+  const NormJob* norms = nullptr;   // up to kMaxNormJobs norm jobs run in the same launch
+  int n_norms = 0;
 };
 
 // One group of query rows attending over [pinned; window; private keys].

@@ -31,7 +31,8 @@ EXPORTS = ("rx_cache_create", "rx_cache_destroy", "rx_pin_prefix", "rx_push_fram
            "rx_set_attn_splits", "rx_launch_count", "rx_status_str", "rx_last_error",
            "rx_attend_regions_static", "rx_attend_suffix_block_causal", "rx_tail_append",
            "rx_snapshot_bytes", "rx_snapshot", "rx_restore", "rx_push_frame_async",
-           "rx_set_attn_dparts", "rx_debug_inject_timeout", "rx_debug_choose_partition")
+           "rx_set_attn_dparts", "rx_debug_inject_timeout", "rx_debug_choose_partition",
+           "rx_attend_suffix_norms", "rx_attend_batch_norms")
 
 
 class RxConfig(ctypes.Structure):
@@ -45,6 +46,13 @@ class RxStreamBatch(ctypes.Structure):
                 ("tail_len", ctypes.c_void_p), ("out", ctypes.c_void_p), ("B", ctypes.c_int),
                 ("T", ctypes.c_int)]
 
+
+class RxNormRows(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("rows", ctypes.c_int), ("d", ctypes.c_int), ("eps", ctypes.c_float)]
+
+
+MAX_NORM_JOBS = 2
 
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _sigs = {
@@ -77,6 +85,9 @@ _sigs = {
     "rx_snapshot": (_i, [_vp, _vp, _vp]),
     "rx_restore": (_i, [_vp, _vp, _vp]),
     "rx_push_frame_async": (_i, [_vp, _vp, _vp, ctypes.POINTER(_i), _vp, _vp]),
+    "rx_attend_suffix_norms": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, ctypes.POINTER(RxNormRows), _i, _vp]),
+    "rx_attend_batch_norms": (_i, [_vp, _i, _vp, _vp, _vp, _i, _vp, ctypes.POINTER(RxStreamBatch),
+                                   ctypes.POINTER(RxNormRows), _i, _vp]),
 }
 for _name, (_res, _args) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -120,6 +131,23 @@ def _shape(t: Optional[torch.Tensor], shape, name: str) -> None:
     caller's buffer)."""
     if t is not None and tuple(t.shape) != tuple(shape):
         raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _norm_jobs(norms) -> Tuple[Optional[ctypes.Array], int]:
+    """norms: a sequence of (x [rows][d] bf16, gamma [d] fp32, eps, y [rows][d]
+    bf16) -> the C array of rx_norm_rows (or None) and its length."""
+    if not norms:
+        return None, 0
+    if len(norms) > MAX_NORM_JOBS:
+        raise ValueError("at most %d norm jobs per launch" % MAX_NORM_JOBS)
+    arr = (RxNormRows * len(norms))()
+    for i, (x, gamma, eps, y) in enumerate(norms):
+        rows, d = x.shape
+        _shape(gamma, (d,), "gamma")
+        _shape(y, x.shape, "y")
+        arr[i] = RxNormRows(_ptr(x, name="x"), _ptr(gamma, torch.float32, "gamma"), _ptr(y, name="y"),
+                            rows, d, float(eps))
+    return arr, len(norms)
 
 
 def launch_count() -> int:
@@ -202,9 +230,11 @@ class Cache:
 
     def attend_suffix(self, layer: int, q: torch.Tensor, k_dyn: torch.Tensor, v_dyn: torch.Tensor,
                       out: Optional[torch.Tensor] = None, stream=None,
-                      n_state: Optional[int] = None) -> torch.Tensor:
+                      n_state: Optional[int] = None, norms=None) -> torch.Tensor:
         """Eq. 1 for one layer; with n_state, the block-causal variant (the
-        first n_state suffix tokens see only their own dynamic keys)."""
+        first n_state suffix tokens see only their own dynamic keys); with
+        norms, a list of up to two (x, gamma, eps, y) AdaRMSNorm jobs run in
+        the same launch (rx_attend_suffix_norms)."""
         c = self.cfg
         S = q.shape[0]
         _shape(q, (S, c.Hq, c.D), "q")
@@ -213,7 +243,14 @@ class Cache:
         _shape(out, q.shape, "out")
         if out is None:
             out = torch.empty_like(q)
-        if n_state is None:
+        if norms:
+            if n_state is not None:
+                raise ValueError("norm jobs run with the plain Eq. 1 call only")
+            arr, n = _norm_jobs(norms)
+            _check(_lib.rx_attend_suffix_norms(self._h, layer, _ptr(q, name="q"), _ptr(k_dyn, name="k_dyn"),
+                                               _ptr(v_dyn, name="v_dyn"), S, _ptr(out, name="out"), arr, n,
+                                               _stream(stream)), "rx_attend_suffix_norms")
+        elif n_state is None:
             _check(_lib.rx_attend_suffix(self._h, layer, _ptr(q, name="q"), _ptr(k_dyn, name="k_dyn"),
                                          _ptr(v_dyn, name="v_dyn"), S, _ptr(out, name="out"),
                                          _stream(stream)), "rx_attend_suffix")
@@ -239,12 +276,14 @@ class Cache:
         _check(_lib.rx_restore(self._h, _ptr(src, torch.uint8, "src"), _stream(stream)), "rx_restore")
 
     def attend_batch(self, layer: int, action=None, lang=None, out_act: Optional[torch.Tensor] = None,
-                     out_lang: Optional[torch.Tensor] = None, stream=None):
+                     out_lang: Optional[torch.Tensor] = None, stream=None, norms=None):
         """One launch for an action suffix and a batch of language streams.
 
         action: (q [S][Hq][D], k_dyn [S][Hkv][D], v_dyn) or None.
         lang: (q [B][T][Hq][D], k_tail [B][tail_cap][Hkv][D], v_tail,
                tail_len int32 CUDA tensor [B]) or None.
+        norms: up to two (x, gamma, eps, y) AdaRMSNorm jobs run in the same
+               launch (rx_attend_batch_norms).
         Returns (out_act or None, out_lang or None).
         """
         c = self.cfg
@@ -272,10 +311,17 @@ class Cache:
             batch = RxStreamBatch(_ptr(ql, name="q_lang"), _ptr(kt, name="k_tail"),
                                   _ptr(vt, name="v_tail"), _ptr(tl, torch.int32, "tail_len"),
                                   _ptr(out_lang, name="out_lang"), ql.shape[0], ql.shape[1])
-        _check(_lib.rx_attend_batch(self._h, layer, _ptr(qa, name="q"), _ptr(kd, name="k_dyn"),
-                                    _ptr(vd, name="v_dyn"), S, _ptr(out_act, name="out_act"),
-                                    ctypes.byref(batch) if batch is not None else None,
-                                    _stream(stream)), "rx_attend_batch")
+        if norms:
+            arr, n = _norm_jobs(norms)
+            _check(_lib.rx_attend_batch_norms(self._h, layer, _ptr(qa, name="q"), _ptr(kd, name="k_dyn"),
+                                              _ptr(vd, name="v_dyn"), S, _ptr(out_act, name="out_act"),
+                                              ctypes.byref(batch) if batch is not None else None,
+                                              arr, n, _stream(stream)), "rx_attend_batch_norms")
+        else:
+            _check(_lib.rx_attend_batch(self._h, layer, _ptr(qa, name="q"), _ptr(kd, name="k_dyn"),
+                                        _ptr(vd, name="v_dyn"), S, _ptr(out_act, name="out_act"),
+                                        ctypes.byref(batch) if batch is not None else None,
+                                        _stream(stream)), "rx_attend_batch")
         return (out_act if action is not None else None), (out_lang if lang is not None else None)
 
     def get_state(self, stream=None) -> Tuple[int, int, int]:
