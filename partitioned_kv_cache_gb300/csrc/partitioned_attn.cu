@@ -158,6 +158,8 @@ struct AttnParams {
   int dparts;            // output columns split over dparts CTAs (each computes S in full)
   int fused;             // 1: the splits of an M-tile form a cluster and merge on chip
   int inject_tx;         // test aid: extra bytes CTA 0 expects on its first K tile
+  int prefetch_l2;       // L2 prefetch before the dependency wait: Q and the split's first
+                         // prefetch_l2 key tiles (0: none)
   float scale_log2;      // log2(e) / sqrt(D)
 };
 
@@ -397,6 +399,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (sg.n_priv > 0) {
       tma_prefetch_desc(&sg.tm_kp);
       tma_prefetch_desc(&sg.tm_vp);
+    }
+    if (p.prefetch_l2) {
+      // A store larger than L2 sends every key tile from DRAM, and the
+      // caller's Q usually too.  Ask for this CTA's Q tile and its split's
+      // first K and V tile to be fetched into L2 now, while the previous
+      // kernel drains.  A prefetch is a hint with no effect on what any load
+      // returns, so it may run before the dependency wait; the ring state is
+      // not read here (it may still be changing), and the first tile is the
+      // one of a full window, clamped inside the regions.
+      for (int kb = 0; kb < Lay::KB; ++kb) tma_prefetch_l2_4d(&sg.tm_q, kb * 64, 0, g, mt * (kBM / p.G));
+      const bool spare = p.slots > p.N;
+      const int wl = (spare ? p.slots - 1 : p.N) * p.F;
+      const int np = (p.P + kBN - 1) / kBN, nw = (wl + kBN - 1) / kBN, nd = (sg.n_priv + kBN - 1) / kBN;
+      const int T = np + nw + nd;
+      const int tf = static_cast<int>(static_cast<unsigned>(split * T) / static_cast<unsigned>(p.n_splits));
+      const int tl = static_cast<int>(static_cast<unsigned>((split + 1) * T) / static_cast<unsigned>(p.n_splits));
+      for (int t = tf; t < tl && t < tf + p.prefetch_l2; ++t) {
+        const TileInfo ti = tile_at(t, np, nw, p.P, wl, sg.n_priv, 0, 0);
+        const uint8_t* kt = ti.region < 2 ? p.k_tiles[ti.region] : nullptr;
+        const uint8_t* vt = ti.region < 2 ? p.v_tiles[ti.region] : nullptr;
+        if (kt && vt) {
+          const long long off = g * p.head_stride[ti.region] + static_cast<long long>(ti.phys0 / kBN) * Lay::TILE;
+          bulk_prefetch_l2(kt + off, static_cast<uint32_t>(Lay::TILE));
+          bulk_prefetch_l2(vt + off + dcol * 128, static_cast<uint32_t>(DV) * 128u);
+        } else if (ti.region == 2) {
+          for (int kb = 0; kb < Lay::KB; ++kb) tma_prefetch_l2_4d(&sg.tm_kp, kb * 64, g, ti.phys0, 0);
+          for (int kb = dcol / 64; kb < (dcol + DV) / 64; ++kb) tma_prefetch_l2_4d(&sg.tm_vp, kb * 64, g, ti.phys0, 0);
+        }
+      }
     }
   }
   // Norm rows of this CTA's softmax warps: fetch the first row and its gamma
@@ -1179,6 +1210,7 @@ cudaError_t launch_partitioned_attention(const AttnLaunch& a, const AttnSegment*
   prm.n_splits = splits;
   prm.dparts = dparts;
   prm.inject_tx = a.inject_tx;
+  prm.prefetch_l2 = a.prefetch_l2;
   prm.fused = fused ? 1 : 0;
   if (used_splits) *used_splits = splits;
   switch (a.D) {

@@ -132,6 +132,9 @@ struct rx_cache {
   int forced_splits = 0;
   int forced_dparts = 0;
   int inject_tx = 0;   // rx_debug_inject_timeout: applies to the next attention launch
+  int prefetch_l2 = 0; // key tiles an attention CTA asks to be fetched into L2 before its
+                       // dependency wait: 1 when the K/V store is larger than half the
+                       // device's L2 (its tiles come from DRAM), else 0
 };
 
 #define RX_GUARD_BEGIN try {
@@ -211,6 +214,10 @@ rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out) {
   const size_t xchg_b = round_up(part_rows * (2 * static_cast<size_t>(c.D) + 8 * 4), 256);
   const size_t st_b = 256;
   h->mem_bytes = 2 * pin_b + 2 * win_b + st_b + xchg_b;
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) l2 = 0;
+  cudaGetLastError();
+  h->prefetch_l2 = l2 > 0 && 2 * (pin_b + win_b) > static_cast<size_t>(l2) / 2 ? 1 : 0;
   e = cudaMalloc(&h->mem, h->mem_bytes);
   if (e != cudaSuccess) {
     delete h;
@@ -377,6 +384,7 @@ static rx::AttnLaunch make_launch(rx_cache_t h, int layer) {
   a.num_sms = h->num_sms;
   a.inject_tx = h->inject_tx;
   h->inject_tx = 0;
+  a.prefetch_l2 = h->prefetch_l2;
   return a;
 }
 

@@ -152,6 +152,9 @@ struct AttnLaunch {
   int inject_tx;      // test aid: extra bytes CTA 0 expects on its first K tile (0 = none)
   const NormJob* norms = nullptr;   // up to kMaxNormJobs norm jobs run in the same launch
   int n_norms = 0;
+  int prefetch_l2 = 0;  // > 0: the store is larger than L2 can keep; each CTA asks for
+                        // its Q tile and its split's first prefetch_l2 key tiles to be
+                        // fetched into L2 while the previous kernel drains
 };
 
 // One group of query rows attending over [pinned; window; private keys].
