@@ -8,7 +8,14 @@ one launch of the attention kernel can be captured in isolation:
     python -m partitioned_kv_cache_gb300.attn_case --workload c4 --layers 2 --calls 6
 
 (--suffix replaces the workload's suffix length, e.g. 1024 query tokens;
---splits and --dparts force the partition, 0 = automatic.)
+--splits and --dparts force the partition, 0 = automatic; --norms runs the
+layer's two AdaRMSNorms of the suffix in the same launch, as the benchmark's
+tick does.)
+
+--op batch runs the shared-cache launch of the workload (the action suffix
+plus its language streams, each with a private tail of U{0..tail_max} keys):
+
+    python -m partitioned_kv_cache_gb300.attn_case --workload c5 --op batch --layers 2 --calls 6
 
 --op gamma issues the gamma-MLP launch of one tick of the workload (all 2L
 norm sites x K steps) a few times, each on its own weight set:
@@ -39,7 +46,8 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", default="c3", choices=sorted(W.WORKLOADS))
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--calls", type=int, default=6)
-    ap.add_argument("--op", default="attention", choices=["attention", "gamma", "push", "norm"])
+    ap.add_argument("--op", default="attention", choices=["attention", "batch", "gamma", "push", "norm"])
+    ap.add_argument("--norms", action="store_true")
     ap.add_argument("--frame-mult", type=int, default=1)
     ap.add_argument("--rows", type=int, default=0)
     ap.add_argument("--suffix", type=int, default=0)
@@ -93,7 +101,8 @@ def main(argv=None) -> None:
         return
 
     S = a.suffix if a.suffix > 0 else wl.S
-    cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, S)
+    B = wl.n_lang if a.op == "batch" else 0
+    cache = rx.Cache(L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, S, wl.tail_cap if B else 0, B)
     cache.set_attn_splits(a.splits)
     cache.set_attn_dparts(a.dparts)
     cache.pin_prefix(r(L, wl.P, wl.Hkv, wl.D), r(L, wl.P, wl.Hkv, wl.D))
@@ -103,13 +112,29 @@ def main(argv=None) -> None:
     kd = r(S, wl.Hkv, wl.D)
     vd = r(S, wl.Hkv, wl.D)
     o = torch.empty_like(q)
+    norms = None
+    if a.norms:
+        gamma = (1.0 + 0.1 * torch.randn(2, wl.d_model, generator=g, device="cuda")).float()
+        x = r(2, S, wl.d_model)
+        y = torch.empty_like(x)
+        norms = [(x[0], gamma[0], wl.eps, y[0]), (x[1], gamma[1], wl.eps, y[1])]
+    if B:
+        lq = r(B, 1, wl.Hq, wl.D)
+        lo = torch.empty_like(lq)
+        tails = (r(B, wl.tail_cap, wl.Hkv, wl.D), r(B, wl.tail_cap, wl.Hkv, wl.D))
+        lens = torch.randint(0, wl.tail_max + 1, (B,), generator=g, device="cuda", dtype=torch.int32)
     for i in range(a.calls):
-        cache.attend_suffix(i % L, q, kd, vd, out=o)
+        if B:
+            cache.attend_batch(i % L, (q, kd, vd), (lq, tails[0], tails[1], lens), out_act=o, out_lang=lo,
+                               norms=norms)
+        else:
+            cache.attend_suffix(i % L, q, kd, vd, out=o, norms=norms)
     torch.cuda.synchronize()
     if cache.check_device_error() != 0:
         raise SystemExit("a kernel reported a device-side timeout")
     cache.close()
-    print("%s: %d attention calls on %d layers" % (wl.name, a.calls, L))
+    print("%s: %d %s calls on %d layers%s" % (wl.name, a.calls, "shared-cache" if B else "attention", L,
+                                             " with two norm jobs each" if norms else ""))
 
 
 if __name__ == "__main__":
