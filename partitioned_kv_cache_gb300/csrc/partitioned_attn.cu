@@ -914,11 +914,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // divided by sum_s w_s, where w_s = 2^(m_s - M) l_s.  A lane pair owns one
 // (row, 16-byte piece): lane 2r + h takes the splits s = h, h + 2, ...  A
 // warp covers 16 consecutive rows of one piece, so its load of one split
-// pair is two runs of 256 contiguous bytes.  Grid: (M-tiles of all segments,
-// pieces, Hkv x dparts), the attention grid's x and z, with 256 threads = 128
-// rows.  Each lane loads up to 16 of its splits at a time, so up to 32 splits
-// are in flight per (row, piece).  More splits run with a running maximum.
-// The pair's (M, L, sums) meet by one shuffle.
+// pair is two runs of 256 contiguous bytes.  A CTA covers 16 rows x 8
+// pieces (its 8 warps, one piece each), so the rows' (m, l) are fetched from
+// L2 once per CTA and served to the other warps from L1.  Grid: (M-tiles of
+// all segments x 8 row groups, pieces / 8, Hkv x dparts), 256 threads.  Each
+// lane loads up to 16 of its splits at a time, so up to 32 splits are in
+// flight per (row, piece).  More splits run with a running maximum.  The
+// pair's (M, L, sums) meet by one shuffle.
 constexpr int kCombineChunk = 16;
 
 template <int D>
@@ -930,20 +932,22 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
   grid_launch_dependents();
   const int DV = D / dparts;
   const int kPieces = DV / 8;
-  const int si = static_cast<int>(blockIdx.x) < m_tiles0 ? 0 : 1;
-  const int mt = blockIdx.x - (si ? m_tiles0 : 0);
+  const int mt_all = blockIdx.x >> 3;                      // M-tile among all segments
+  const int m_total = gridDim.x >> 3;
+  const int si = mt_all < m_tiles0 ? 0 : 1;
+  const int mt = mt_all - (si ? m_tiles0 : 0);
   const int rows = si ? rows1 : rows0;
   __nv_bfloat16* out = si ? out1 : out0;
   const int lane = threadIdx.x & 31;
   const int half = lane & 1;
-  const int i = (threadIdx.x >> 5) * 16 + (lane >> 1);   // row within the tile
-  const int k = blockIdx.y;                                // piece
+  const int i = (blockIdx.x & 7) * 16 + (lane >> 1);      // row within the tile
+  const int k = blockIdx.y * 8 + (threadIdx.x >> 5);       // piece
   const int Rs = mt * kBM + i;
   const bool live_row = Rs < rows;   // padding rows were never written: their loads stay in the tile
   const int C = n_splits;
-  const size_t cid = static_cast<size_t>(blockIdx.z) * gridDim.x + blockIdx.x;
+  const size_t cid = static_cast<size_t>(blockIdx.z) * m_total + mt_all;
   const uint4* src = xchg + cid * C * kPieces * kBM + static_cast<size_t>(k) * kBM + i;
-  const float2* ml_src = reinterpret_cast<const float2*>(xchg + static_cast<size_t>(gridDim.x) * gridDim.z * C *
+  const float2* ml_src = reinterpret_cast<const float2*>(xchg + static_cast<size_t>(m_total) * gridDim.z * C *
                                                                     kPieces * kBM) +
                          cid * C * kBM + i;
   float M = -INFINITY, L = 0.f;
@@ -958,7 +962,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const uint4* __restri
       const int s = s0 + 2 * u;
       const bool use = live_row && s < C;
       pv[u] = use ? __ldcg(src + static_cast<size_t>(s) * kPieces * kBM) : make_uint4(0u, 0u, 0u, 0u);
-      ml[u] = use ? __ldcg(ml_src + static_cast<size_t>(s) * kBM) : make_float2(-INFINITY, 0.f);
+      ml[u] = use ? ml_src[static_cast<size_t>(s) * kBM] : make_float2(-INFINITY, 0.f);   // L1: 8 warps read it
     }
     float mc = -INFINITY;
 #pragma unroll
@@ -1039,7 +1043,7 @@ cudaError_t launch_one(const AttnParams& prm, int m_tiles, int Hkv, cudaStream_t
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || prm.n_splits == 1 || prm.fused) return e;
-  dim3 cgrid(m_tiles, D / prm.dparts / 8, Hkv * prm.dparts);
+  dim3 cgrid(m_tiles * 8, D / prm.dparts / 64, Hkv * prm.dparts);
   e = launch_k(attn_combine_kernel<D>, cgrid, dim3(256), 0, s, static_cast<const uint4*>(prm.xchg),
                prm.seg[0].out, prm.seg[0].rows, prm.seg[0].m_tiles, prm.seg[1].out, prm.seg[1].rows,
                prm.n_splits, prm.dparts, prm.Hq, prm.G);
