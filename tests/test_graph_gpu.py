@@ -92,3 +92,85 @@ def test_replayed_tick_matches_the_oracle(rx, spare):
     assert cache.debug_window() is not None
     assert cache.check_device_error() == 0
     cache.close()
+
+
+def test_replayed_benchmark_tick_matches_the_oracle_stream(rx):
+    """The benchmark's tick, captured once and replayed tick after tick: one
+    gamma launch for every (layer, site, step), the frame push, then per step
+    and layer one launch of the attention with the layer's two AdaRMSNorms
+    (rx_attend_suffix_norms).  After every replay each of the three outputs
+    of every (step, layer) is compared with the oracle's stream tick ("Reflex
+    ...", §III Eq. (1) and Eq. (2)): the norms within the norm tolerance, the
+    attention within the attention tolerance."""
+    import torch
+    from tests._util import check_norm
+    wl = W.Workload("tick-2L", L=2, Hq=8, Hkv=1, D=256, P=64, N=3, F=256, S=51, steps=3, ticks=1,
+                    d_model=1024, emb_dim=16, state_dim=16, hidden=512)
+    seed = 22
+    cache = rx.Cache(wl.L, wl.Hq, wl.Hkv, wl.D, wl.P, wl.N, wl.F, wl.S)
+    pk, pv = W.pinned_kv(wl, seed)
+    cache.pin_prefix(dev(pk), dev(pv))
+    ost = OracleStream(wl, seed)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    K, L = wl.steps, wl.L
+    fk = torch.empty((L, wl.F, wl.Hkv, wl.D), **bf)
+    fv = torch.empty_like(fk)
+    q = torch.empty((K, L, wl.S, wl.Hq, wl.D), **bf)
+    kd = torch.empty((K, L, wl.S, wl.Hkv, wl.D), **bf)
+    vd = torch.empty_like(kd)
+    x = torch.empty((K, L, 2, wl.S, wl.d_model), **bf)
+    o = torch.empty_like(q)
+    y = torch.empty_like(x)
+    mlp = [W.mlp_weights(wl, seed, l, site) for l in range(L) for site in (0, 1)]
+    W1, b1, W2, b2 = (torch.stack([dev(m[i]) for m in mlp]) for i in range(4))
+    tk = torch.tensor(W.timesteps(wl), device="cuda")
+    state = torch.empty((K, wl.state_dim), dtype=torch.float32, device="cuda")
+    gamma = torch.empty((2 * L, K, wl.d_model), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def load(t):
+        a, b = W.frame_kv(wl, seed, t)
+        fk.copy_(dev(a))
+        fv.copy_(dev(b))
+        state.copy_(torch.from_numpy(np.tile(W.robot_state(wl, seed, t), (K, 1))).cuda())
+        for k in range(K):
+            for l in range(L):
+                qq, kk, vv = W.suffix_qkv(wl, seed, t, k, l)
+                q[k, l].copy_(dev(qq))
+                kd[k, l].copy_(dev(kk))
+                vd[k, l].copy_(dev(vv))
+                for site in (0, 1):
+                    x[k, l, site].copy_(dev(W.norm_input(wl, seed, t, k, l, site)))
+
+    def tick():
+        rx.ada_gamma(tk, state, W1, b1, W2, b2, wl.emb_dim, out=gamma)
+        cache.push_frame(fk, fv)
+        for k in range(K):
+            for l in range(L):
+                cache.attend_suffix(l, q[k, l], kd[k, l], vd[k, l], out=o[k, l],
+                                    norms=[(x[k, l, 0], gamma[2 * l, k], wl.eps, y[k, l, 0]),
+                                           (x[k, l, 1], gamma[2 * l + 1, k], wl.eps, y[k, l, 1])])
+
+    def check(t):
+        want = ost.tick(t)
+        for (k, l), (y0, att, y1) in want.items():
+            check_norm(host64(y[k, l, 0]), y0)
+            check_attention(host64(o[k, l]), att)
+            check_norm(host64(y[k, l, 1]), y1)
+
+    with torch.cuda.stream(s):   # tick 0 eagerly (first launches set kernel attributes)
+        load(0)
+        tick()
+    torch.cuda.synchronize()
+    check(0)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        tick()
+    for t in range(1, wl.N + 3):
+        with torch.cuda.stream(s):
+            load(t)
+            gr.replay()
+        torch.cuda.synchronize()
+        check(t)
+    assert cache.check_device_error() == 0
+    cache.close()
