@@ -436,14 +436,22 @@ def run_ours(args, wl):
             tick(s)
         graphs.append(gr)
     launches_per_tick = (rx.launch_count() - n0) // NSLOT
-    a_graph = torch.cuda.CUDAGraph()
+    # The tick's launches without the gamma and the push, one graph per input
+    # slot, replayed alternately as the ticks are (the slots' inputs do not
+    # stay in L2): with the norm jobs (the tick's launch) and without.
+    a_graphs, p_graphs = [], []
     n1 = rx.launch_count()
-    with torch.cuda.graph(a_graph, stream=stream):
-        attn_only(0)
-    attn_kernels_per_call = (rx.launch_count() - n1) / (K * L)
-    p_graph_attn = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(p_graph_attn, stream=stream):
-        attn_only(0, fused=False)
+    for s in range(NSLOT):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            attn_only(s)
+        a_graphs.append(gr)
+    attn_kernels_per_call = (rx.launch_count() - n1) / (NSLOT * K * L)
+    for s in range(NSLOT):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            attn_only(s, fused=False)
+        p_graphs.append(gr)
     torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -492,28 +500,24 @@ def run_ours(args, wl):
     del sep_graph
 
     # ---------------- attention alone: per-launch time for the roofline ----------------
-    reps = max(3, min(50, args.steps // 10))
-    with torch.cuda.stream(stream):
-        a_graph.replay()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(reps):
-            a_graph.replay()
-        a1.record(stream)
-    a1.synchronize()
-    attn_us = a0.elapsed_time(a1) * 1e3 / (reps * K * L)
-    with torch.cuda.stream(stream):
-        p_graph_attn.replay()
-        a2 = torch.cuda.Event(enable_timing=True)
-        a3 = torch.cuda.Event(enable_timing=True)
-        a2.record(stream)
-        for _ in range(reps):
-            p_graph_attn.replay()
-        a3.record(stream)
-    a3.synchronize()
-    plain_us = a2.elapsed_time(a3) * 1e3 / (reps * K * L)
-    del p_graph_attn
+    reps = 2 * max(2, min(25, args.steps // 20))
+
+    def per_call_us(grs):
+        with torch.cuda.stream(stream):
+            for gr in grs:
+                gr.replay()
+            b0 = torch.cuda.Event(enable_timing=True)
+            b1 = torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for i in range(reps):
+                grs[i % NSLOT].replay()
+            b1.record(stream)
+        b1.synchronize()
+        return b0.elapsed_time(b1) * 1e3 / (reps * K * L)
+
+    attn_us = per_call_us(a_graphs)
+    plain_us = per_call_us(p_graphs)
+    del a_graphs, p_graphs
     fl = attn_flops(wl)
     achieved = fl / (attn_us * 1e-6) / 1e12
     peak_tf = float(peaks["bf16_tflops"])

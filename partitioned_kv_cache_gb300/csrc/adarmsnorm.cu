@@ -73,8 +73,9 @@ __global__ void __launch_bounds__(256) adarmsnorm_kernel(const uint4* __restrict
 }
 
 // ---------------------------------------------------------------- gamma MLP
-// The first layer and the SiLU run on the CUDA cores in fp32 (each CTA
-// recomputes h for its weight set: 16K multiply-adds per vector).  The second
+// The first layer and the SiLU run on the CUDA cores in fp32, shared out over
+// the cluster of the weight set's row tiles (each CTA computes 1/8 of h and
+// copies it into its peers' shared memory).  The second
 // layer runs on the tensor cores: per weight set, W2 [d x hidden] times H^T,
 // where the rows of H are the hidden activations of the conditioning vectors.
 // One CTA computes 128 rows of W2 against every vector (tcgen05 M = 128,
@@ -101,6 +102,7 @@ struct GammaArgs {
   const __nv_bfloat16* b2;
   float* gamma;
   int n_cond, emb_dim, state_dim, hidden, d;
+  int cluster;         // CTAs of one weight set (row tiles) that share the first layer
 };
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
@@ -161,55 +163,60 @@ __global__ void __launch_bounds__(kGThreads, 1) ada_gamma_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // No early release of the next kernel (griddepcontrol.launch_dependents):
+  // as with the ring append, an attention chain released early behind a
+  // launch that holds the SMs' shared memory ran ~1 us slower per launch.
   grid_dependency_wait();
-  grid_launch_dependents();
 
-  // The small inputs are requested before W2: the 1 MB per set of W2 fills
-  // the DRAM queues for microseconds, and anything requested behind it waits
-  // that long.  This thread's first kPreRows rows of W1 and b1, its output
-  // row's b2 and its share of t and state go first; the common shapes
-  // (hidden <= 512, cond width <= 32, n_cond * cond width <= 512) need no
-  // other load before the MMAs.
-  constexpr int kPreRows = 2;
+  // The first layer is shared out over the cluster of the weight set's row
+  // tiles: CTA `crank` of `csize` computes the 64-unit blocks kb of h with
+  // kb % csize == crank and copies each into its peers' H operand, so each
+  // CTA computes 1/csize of the layer instead of all of it.  Within a block,
+  // thread t takes unit kb * 64 + (t % 64) and the vectors k = t / 64 + 4i.
+  const int crank = a.cluster > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int csize = a.cluster;
+  const int ju = threadIdx.x & 63, kq = threadIdx.x >> 6;
   const __nv_bfloat16* W1s = a.W1 + static_cast<size_t>(set) * a.hidden * cond_dim;
   const __nv_bfloat16* b1s = a.b1 + static_cast<size_t>(set) * a.hidden;
   const bool w1_fast = (cond_dim & 7) == 0 && cond_dim <= 32 && (reinterpret_cast<uintptr_t>(W1s) & 15) == 0;
+
+  // The small inputs are requested before W2: the 1 MB per set of W2 fills
+  // the DRAM queues for microseconds, and anything requested behind it waits
+  // that long.  This thread's row of W1 in its first block, its b1, its
+  // output row's b2 go first, and W2 is requested once thread 0's have
+  // arrived.
   // (kept as raw bf16 until used: converting at the load would wait for it)
-  uint4 w1v[kPreRows][4];
-  __nv_bfloat16 b1v[kPreRows];
+  uint4 w1v[4];
+  const int j0 = crank * 64 + ju;                           // this thread's unit in its first block
+  const bool have0 = crank < nkb && j0 < a.hidden;
+  __nv_bfloat16 b1v = __float2bfloat16_rn(0.f);
+  if (w1_fast && have0) {
+    const uint4* src = reinterpret_cast<const uint4*>(W1s + static_cast<size_t>(j0) * cond_dim);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (8 * u < cond_dim) w1v[u] = __ldg(src + u);
+    b1v = b1s[j0];
+  }
   const int i_out = tile * kGM + (warp & 3) * 32 + lane;   // this thread's output row (epilogue)
   const __nv_bfloat16 b2v = a.b2[static_cast<size_t>(set) * a.d + (i_out < a.d ? i_out : a.d - 1)];
-#pragma unroll
-  for (int r = 0; r < kPreRows; ++r) {
-    const int j = threadIdx.x + r * kGThreads;
-    b1v[r] = __float2bfloat16_rn(0.f);
-    if (w1_fast && j < a.hidden) {
-      const uint4* src = reinterpret_cast<const uint4*>(W1s + static_cast<size_t>(j) * cond_dim);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (8 * u < cond_dim) w1v[r][u] = __ldg(src + u);
-      b1v[r] = b1s[j];
-    }
-  }
-
-  // c_k = [sin(t_k w_j), cos(t_k w_j), state_k],  w_j = 10000^(-j/half):
-  // element idx of c reads t[k] (embedding) or one state value.
-  constexpr int kPreC = 2;
-  float cin[kPreC];
-#pragma unroll
-  for (int r = 0; r < kPreC; ++r) {
-    const int idx = threadIdx.x + r * kGThreads;
-    cin[r] = 0.f;
-    if (idx < a.n_cond * cond_dim) {
-      const int k = idx / cond_dim, j = idx - k * cond_dim;
-      cin[r] = j < a.emb_dim ? a.t[k] : a.state[k * a.state_dim + (j - a.emb_dim)];
-    }
-  }
+  // The conditioning inputs of this thread's first element of c: a time
+  // (embedding pairs) and a state value.
+  const int half = a.emb_dim / 2;
+  const float t_in = threadIdx.x < a.n_cond * half ? a.t[threadIdx.x / half] : 0.f;
+  const float s_in = threadIdx.x < a.n_cond * a.state_dim ? a.state[threadIdx.x] : 0.f;
   __syncthreads();   // every small load is out before W2 is requested
   // W2 blocks 0..kGSlots-1 go out first, the rest to L2; h is computed while
   // they land.
   int issued = 0;
   if (threadIdx.x == 0) {
+    if (w1_fast && have0) {
+      uint32_t dep = __bfloat16_as_ushort(b2v) ^ __bfloat16_as_ushort(b1v) ^ __float_as_uint(t_in) ^
+                     __float_as_uint(s_in);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (8 * u < cond_dim) dep ^= w1v[u].x ^ w1v[u].w;
+      asm volatile("" ::"r"(dep));
+    }
     for (; issued < kGSlots && issued < nkb; ++issued) {
       mbar_arrive_expect_tx(FULL(issued), kGBlock);
       tma_load_4d(sRing + issued * kGBlock, &a.tm_w2, issued * 64, tile * kGM, set, 0, FULL(issued));
@@ -217,85 +224,107 @@ __global__ void __launch_bounds__(kGThreads, 1) ada_gamma_kernel(const __grid_co
     for (int b = kGSlots; b < nkb; ++b) tma_prefetch_l2_4d(&a.tm_w2, b * 64, tile * kGM, set, 0);
   }
 
-  const int half = a.emb_dim / 2;
-  auto c_elem = [&](int idx, float in) {
-    const int k = idx / cond_dim, j = idx - k * cond_dim;
-    float v = in;
-    if (j < a.emb_dim) {
-      const int jj = j < half ? j : j - half;
-      const float w = powf(10000.0f, -static_cast<float>(jj) / static_cast<float>(half));
-      v = j < half ? sinf(in * w) : cosf(in * w);
-    }
-    c[k * c_stride + j] = v;
-  };
-#pragma unroll
-  for (int r = 0; r < kPreC; ++r)
-    if (threadIdx.x + r * kGThreads < a.n_cond * cond_dim) c_elem(threadIdx.x + r * kGThreads, cin[r]);
-  for (int idx = threadIdx.x + kPreC * kGThreads; idx < a.n_cond * cond_dim; idx += blockDim.x) {
-    const int k = idx / cond_dim, j = idx - k * cond_dim;
-    c_elem(idx, j < a.emb_dim ? a.t[k] : a.state[k * a.state_dim + (j - a.emb_dim)]);
+  // c_k = [sin(t_k w_j), cos(t_k w_j), state_k],  w_j = 10000^(-j/half):
+  // one sincos per (vector, frequency), the state copied.
+  for (int idx = threadIdx.x; idx < a.n_cond * half; idx += blockDim.x) {
+    const int k = idx / half, jj = idx - k * half;
+    const float w = powf(10000.0f, -static_cast<float>(jj) / static_cast<float>(half));
+    float sv, cv;
+    sincosf((idx == threadIdx.x ? t_in : a.t[k]) * w, &sv, &cv);
+    c[k * c_stride + jj] = sv;
+    c[k * c_stride + half + jj] = cv;
   }
-  // H starts as zeros: unused vectors, and columns past hidden in the last block.
-  for (int o = threadIdx.x * 16; o < nkb * kGHBlock; o += blockDim.x * 16)
-    st_shared_v4(sH + o, 0u, 0u, 0u, 0u);
+  for (int idx = threadIdx.x; idx < a.n_cond * a.state_dim; idx += blockDim.x) {
+    const int k = idx / a.state_dim, e = idx - k * a.state_dim;
+    c[k * c_stride + a.emb_dim + e] = idx == threadIdx.x ? s_in : a.state[idx];
+  }
+  // This CTA's blocks of H start as zeros: unused vectors, and columns past
+  // hidden in the last block.  Blocks owned by a peer are written whole by it.
+  for (int kb = crank; kb < nkb; kb += csize) st_shared_v4(sH + kb * kGHBlock + threadIdx.x * 16, 0u, 0u, 0u, 0u);
   __syncthreads();
 
   // h_k = SiLU(W1 c_k + b1) in fp32, stored as hi / lo bf16 rows of H.
-  int j_rest = 0;   // first row not covered by the preloaded ones
-  if (w1_fast) {
+  for (int kb = crank; kb < nkb; kb += csize) {
+    const int j = kb * 64 + ju;
+    if (j >= a.hidden) continue;
+    float acc[kMaxCond / 4];
 #pragma unroll
-    for (int r = 0; r < kPreRows; ++r) {
-      const int j = threadIdx.x + r * kGThreads;
-      if (j < a.hidden) {
-        float acc[kMaxCond];
+    for (int i = 0; i < kMaxCond / 4; ++i) acc[i] = 0.f;
+    if (w1_fast) {
+      uint4 wv[4];
+      if (kb == crank) {
 #pragma unroll
-        for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
+        for (int u = 0; u < 4; ++u) wv[u] = w1v[u];
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(W1s + static_cast<size_t>(j) * cond_dim);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (8 * u < cond_dim) {
-            float w[8];
-            unpack8(w1v[r][u], w);
+        for (int u = 0; u < 4; ++u)
+          if (8 * u < cond_dim) wv[u] = __ldg(src + u);
+      }
 #pragma unroll
-            for (int k = 0; k < kMaxCond; ++k) {
-              if (k < a.n_cond) {
-                const float4 c0 = *reinterpret_cast<const float4*>(c + k * c_stride + 8 * u);
-                const float4 c1 = *reinterpret_cast<const float4*>(c + k * c_stride + 8 * u + 4);
-                acc[k] = fmaf(w[0], c0.x, fmaf(w[1], c0.y, fmaf(w[2], c0.z, fmaf(w[3], c0.w, acc[k]))));
-                acc[k] = fmaf(w[4], c1.x, fmaf(w[5], c1.y, fmaf(w[6], c1.z, fmaf(w[7], c1.w, acc[k]))));
-              }
+      for (int u = 0; u < 4; ++u) {
+        if (8 * u < cond_dim) {
+          float w[8];
+          unpack8(wv[u], w);
+#pragma unroll
+          for (int i = 0; i < kMaxCond / 4; ++i) {
+            const int k = kq + 4 * i;
+            if (k < a.n_cond) {
+              const float4 c0 = *reinterpret_cast<const float4*>(c + k * c_stride + 8 * u);
+              const float4 c1 = *reinterpret_cast<const float4*>(c + k * c_stride + 8 * u + 4);
+              acc[i] = fmaf(w[0], c0.x, fmaf(w[1], c0.y, fmaf(w[2], c0.z, fmaf(w[3], c0.w, acc[i]))));
+              acc[i] = fmaf(w[4], c1.x, fmaf(w[5], c1.y, fmaf(w[6], c1.z, fmaf(w[7], c1.w, acc[i]))));
             }
           }
         }
+      }
+    } else {   // wider or unaligned first layers
+      const __nv_bfloat16* wr = W1s + static_cast<size_t>(j) * cond_dim;
+      for (int e = 0; e < cond_dim; ++e) {
+        const float w = __bfloat162float(wr[e]);
 #pragma unroll
-        for (int k = 0; k < kMaxCond; ++k) {
-          if (k < a.n_cond) {
-            const float z = acc[k] + __bfloat162float(b1v[r]);
-            store_h(sH, j, k, __fdividef(z, 1.0f + __expf(-z)));
-          }
+        for (int i = 0; i < kMaxCond / 4; ++i) {
+          const int k = kq + 4 * i;
+          if (k < a.n_cond) acc[i] = fmaf(w, c[k * c_stride + e], acc[i]);
         }
       }
     }
-    j_rest = kPreRows * kGThreads;
-  }
-  for (int j = j_rest + threadIdx.x; j < a.hidden; j += blockDim.x) {   // wider shapes
-    float acc[kMaxCond];
+    const float bias = __bfloat162float(w1_fast && kb == crank ? b1v : b1s[j]);
 #pragma unroll
-    for (int k = 0; k < kMaxCond; ++k) acc[k] = 0.f;
-    const __nv_bfloat16* wr = W1s + static_cast<size_t>(j) * cond_dim;
-    for (int e = 0; e < cond_dim; ++e) {
-      const float w = __bfloat162float(wr[e]);
-#pragma unroll
-      for (int k = 0; k < kMaxCond; ++k)
-        if (k < a.n_cond) acc[k] = fmaf(w, c[k * c_stride + e], acc[k]);
-    }
-    const float bias = __bfloat162float(b1s[j]);
-#pragma unroll
-    for (int k = 0; k < kMaxCond; ++k) {
+    for (int i = 0; i < kMaxCond / 4; ++i) {
+      const int k = kq + 4 * i;
       if (k < a.n_cond) {
-        const float z = acc[k] + bias;
+        const float z = acc[i] + bias;
         store_h(sH, j, k, __fdividef(z, 1.0f + __expf(-z)));
       }
     }
+  }
+  if (csize > 1) {
+    // The rows of each own block that hold vectors (hi rows k < n_cond and
+    // lo rows 16 + k, 128 bytes each; one 16-byte chunk per thread) go to
+    // the same place in every peer's H.  A peer's other rows feed only
+    // columns of the product that are never read.  Then one cluster barrier:
+    // after it every CTA holds all of H, and no peer writes into this CTA's
+    // shared memory any more.
+    __syncthreads();
+    const int n_rows = 2 * a.n_cond;
+    const int row = threadIdx.x >> 3;                       // 0..31
+    const bool used = threadIdx.x < 8 * 32 && (row < a.n_cond || (row >= 16 && row < 16 + a.n_cond));
+    for (int kb = crank; kb < nkb && used && n_rows > 0; kb += csize) {
+      const uint32_t src = sH + kb * kGHBlock + threadIdx.x * 16;
+      uint32_t v0, v1, v2, v3;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(src));
+      for (int pr = 0; pr < csize; ++pr) {
+        if (pr == crank) continue;
+        uint32_t dst;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(src), "r"(pr));
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v0), "r"(v1), "r"(v2),
+                     "r"(v3)
+                     : "memory");
+      }
+    }
+    asm volatile("fence.proxy.async;" ::: "memory");   // this thread's H stores -> tensor-core reads
+    cluster_sync_all();
   }
   fence_proxy_async_smem();   // H (generic-proxy stores) -> tensor-core reads
   __syncthreads();
@@ -420,8 +449,31 @@ cudaError_t launch_ada_gamma(const float* t, const float* state, int n_cond, int
   cudaError_t e = cudaFuncSetAttribute(ada_gamma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const dim3 grid((d + kGM - 1) / kGM, n_sets);
-  e = launch_k(ada_gamma_kernel, grid, dim3(kGThreads), smem, s, a);
+  // The row tiles of one weight set share the first layer as one cluster of
+  // up to 8 CTAs (the largest of 8, 4, 2 that divides the tile count).
+  const int tiles = (d + kGM - 1) / kGM;
+  a.cluster = tiles % 8 == 0 ? 8 : tiles % 4 == 0 ? 4 : tiles % 2 == 0 ? 2 : 1;
+  const dim3 grid(tiles, n_sets);
+  if (a.cluster == 1) {
+    e = launch_k(ada_gamma_kernel, grid, dim3(kGThreads), smem, s, a);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = a.cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, ada_gamma_kernel, a);
+    count_launch();
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -48,12 +48,18 @@ __device__ __forceinline__ long long tiled_offset(int l, int g, int Hkv, int T, 
          ((cb ^ (r & 7)) << 4);
 }
 
+// Neither packing kernel lets the next kernel launch early (no
+// griddepcontrol.launch_dependents: the next kernel is released when this
+// grid completes).  Measured on GB300 with a tick of the long-history stack:
+// when a push released the attention chain after it early, the attention
+// launches of the whole tick took ~1 us longer each (2.41 against 2.20 ms
+// a tick); the chain's CTAs are launched while the push's CTAs still hold
+// the SMs' shared memory.
 __global__ void __launch_bounds__(kThreads) pack_tiles_kernel(
     const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint8_t* __restrict__ k_dst,
     uint8_t* __restrict__ v_dst, int L, int n, int Hkv, int D, int T, int tok0, DevState* st,
     int F, int N, int slots) {
   grid_dependency_wait();
-  grid_launch_dependents();
   // A ring append reads the state before any CTA can update it (the update
   // waits for every CTA to arrive).
   int head = 0, valid = 0;
@@ -186,8 +192,7 @@ __global__ void __launch_bounds__(32) pack_tiles_tma_kernel(const __grid_constan
   // L2 rather than DRAM.
   if (threadIdx.x == 0)
     for (int kb = 0; kb < a.D / 64; ++kb) tma_prefetch_l2_4d(&a.tm[kv], kb * 64, g, blockIdx.x * kTileTok, l);
-  grid_dependency_wait();
-  grid_launch_dependents();
+  grid_dependency_wait();   // no early release of the next kernel (see pack_tiles_kernel)
   if (threadIdx.x != 0) return;
   const uint32_t bytes = static_cast<uint32_t>(tile_bytes(a.D));
   // The source boxes do not depend on the ring state: issue them first and
