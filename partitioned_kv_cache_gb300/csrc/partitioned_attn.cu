@@ -733,13 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         __nv_bfloat16* dst = sg.out + (static_cast<size_t>(tok) * p.Hq + h) * D + dcol;
         const float inv = l > 0.f ? 1.f / l : 0.f;   // a row with no key at all gets zeros
 #pragma unroll 1
-        for (int c = 0; c < DV; c += 32) {
-          float o[32];
-          tmem_ld32(tO + c + lane_off, o);
+        for (int c = 0; c < DV; c += 64) {   // 64 columns per TMEM load: half the round trips
+          float o[64];
+          tmem_ld64(tO + c + lane_off, o);
           if (row_valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
               d4[i] = make_uint4(pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv),
                                  pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
                                  pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
@@ -757,12 +757,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const float inv = l > 0.f ? 1.f / l : 0.f;
         uint4* dst = xchg_o(p, DV, split) + row;
 #pragma unroll 1
-        for (int c = 0; c < DV; c += 32) {
-          float o[32];
-          tmem_ld32(tO + c + lane_off, o);
+        for (int c = 0; c < DV; c += 64) {   // 64 columns per TMEM load: half the round trips
+          float o[64];
+          tmem_ld64(tO + c + lane_off, o);
           if (row_valid) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 8; ++q)
               dst[static_cast<size_t>(c / 8 + q) * kBM] =
                   make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
                              pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
@@ -807,17 +807,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       const float inv = fin_l > 0.f ? 1.f / fin_l : 0.f;
       uint4* dst = xo + static_cast<size_t>(rank) * kPieces * kBM + row;
 #pragma unroll 1
-      for (int c = 0; c < DV; c += 32) {
-        float o[32];
+      for (int c = 0; c < DV; c += 64) {   // 64 columns per TMEM load: half the round trips
+        float o[64];
         if (fin_have) {   // warp-uniform: the TMEM load is warp-collective
-          tmem_ld32(tO + c + lane_off, o);
+          tmem_ld64(tO + c + lane_off, o);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+          for (int e = 0; e < 64; ++e) o[e] = 0.f;
         }
         if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 8; ++q)
             dst[static_cast<size_t>(c / 8 + q) * kBM] =
                 make_uint4(pack_bf16x2(o[8 * q] * inv, o[8 * q + 1] * inv),
                            pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
