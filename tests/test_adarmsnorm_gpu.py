@@ -77,6 +77,8 @@ def test_zero_rows_is_a_noop(rx):
     (136, 2048, 6, 5, 1, 1.0),       # widest hidden; conditioning width 11 (not a multiple of 8)
     (8, 16, 2, 0, 5, 1.0),           # smallest shapes, no state
     (256, 512, 16, 16, 10, 50.0),    # weights ~N(0, 1): gamma - 1 of order 100
+    (512, 256, 16, 16, 3, 1.0),      # 4 row tiles: a cluster of 4 sharing 4 blocks of the first layer
+    (384, 192, 16, 16, 7, 1.0),      # 3 row tiles: no cluster, every CTA computes all 3 blocks
 ])
 def test_gamma_shapes_and_scales(rx, d, hidden, emb, state_dim, n_cond, wscale):
     """Eq. (2)'s gamma MLP over the edge shapes of the kernel.  Bound: the

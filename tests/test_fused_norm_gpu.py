@@ -64,20 +64,23 @@ def _check_jobs(rx, jobs, host):
         assert torch.equal(y, rx.adarmsnorm(x, g, eps)), "fused norm differs from rx_adarmsnorm"
 
 
-@pytest.mark.parametrize("name,shapes", [
-    ("c3", [(51, 1024), (51, 1024)]),          # the benchmark's two norms per layer
-    ("c4", [(51, 1024), (51, 1024)]),          # unclustered partition + combine kernel
-    ("c2", [(700, 1024), (900, 1024)]),        # more rows than the launch has softmax warps
-    ("c2", [(51, 128), (0, 1024)]),            # a narrow row, an empty job
-    ("c2", [(37, 2048)]),                      # wide rows: the two-pass form
+@pytest.mark.parametrize("name,shapes,splits", [
+    ("c3", [(51, 1024), (51, 1024)], 0),          # the benchmark's two norms per layer
+    ("c4", [(51, 1024), (51, 1024)], 0),          # unclustered partition + combine kernel
+    ("c2", [(700, 1024), (900, 1024)], 0),        # more rows than the launch has softmax warps
+    ("c2", [(51, 128), (0, 1024)], 0),            # a narrow row, an empty job
+    ("c2", [(37, 2048)], 0),                      # wide rows: the two-pass form
+    ("c2", [(51, 1024), (51, 1024)], 1),          # one split: the CTAs write the output themselves
+    ("c2", [(51, 1024), (51, 1024)], 17),         # more splits than a cluster: the combine kernel
 ])
-def test_suffix_with_norm_jobs(rx, name, shapes):
+def test_suffix_with_norm_jobs(rx, name, shapes, splits):
     import dataclasses
     wl = W.WORKLOADS[name]
     if wl.L > 2:
         wl = dataclasses.replace(wl, L=2)
     seed = 51
     cache, ost = _store(rx, wl, seed, wl.N + 1)
+    cache.set_attn_splits(splits)
     f = W.bf16_bits_to_f64
     for layer in range(wl.L):
         q, kd, vd = W.suffix_qkv(wl, seed, wl.N, 0, layer)
