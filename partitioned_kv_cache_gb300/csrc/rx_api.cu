@@ -536,6 +536,13 @@ struct SnapHeader {
 static_assert(sizeof(SnapHeader) <= 256, "snapshot header");
 constexpr long long kSnapHeader = 256;
 
+// Writes a snapshot's header: the values travel as the kernel's argument, so
+// nothing on the host has to outlive the call (the same holds under stream
+// capture).
+__global__ void snapshot_header_kernel(const __grid_constant__ SnapHeader hd, SnapHeader* dst) {
+  if (threadIdx.x == 0) *dst = hd;
+}
+
 long long snapshot_body(rx_cache_t h) {
   return reinterpret_cast<const char*>(h->dstate) + sizeof(rx::DevState) -
          reinterpret_cast<const char*>(h->k_pin);
@@ -562,8 +569,9 @@ rx_status rx_snapshot(rx_cache_t h, void* dst, void* stream) {
   hd.host_pushes = h->host_pushes;
   hd.body_bytes = snapshot_body(h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The header is staged from pageable memory before the call returns.
-  cudaError_t e = cudaMemcpyAsync(dst, &hd, sizeof(hd), cudaMemcpyHostToDevice, s);
+  snapshot_header_kernel<<<1, 32, 0, s>>>(hd, static_cast<SnapHeader*>(dst));
+  rx::count_launch();
+  cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(static_cast<char*>(dst) + kSnapHeader, h->k_pin, hd.body_bytes,
                         cudaMemcpyDeviceToDevice, s);
