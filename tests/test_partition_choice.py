@@ -34,7 +34,7 @@ def choose(rx, t_max, units, D=256, splits=0, dparts=0, max_splits=MAX_SPLITS, c
     # 51 tokens x 8 heads = 4 query tiles; key tiles = pinned + window + dynamic
     ("c2: 48 + 4x256 + 51 keys", 1 + 16 + 1, 4, (12, 2, True)),
     ("c3: 64 + 8x256 + 51 keys", 1 + 32 + 1, 4, (12, 2, True)),
-    ("c4: 256 + 32x256 + 51 keys", 4 + 128 + 1, 4, (28, 1, False)),
+    ("c4: 256 + 32x256 + 51 keys", 4 + 128 + 1, 4, (27, 1, False)),
     ("c5: c3 + 16 language tails of 32", 1 + 32 + 8, 5, (16, 1, True)),
     ("1024-token suffix over c3's keys", 1 + 32 + 16, 64, (2, 1, True)),
     ("2048-token suffix over c4's keys", 4 + 128 + 32, 128, (1, 1, False)),
