@@ -211,7 +211,9 @@ typedef struct rx_norm_rows {
  * rx_adarmsnorm on the same arguments.  The norm rows run on the attention
  * CTAs' softmax warps while those wait for their first score tile.  The jobs
  * must not read what the attention call writes or write what it reads (the
- * launch runs both at once).  n_norms = 0 is rx_attend_suffix.
+ * launch runs both at once): a job whose y overlaps q, k_dyn, v_dyn or out,
+ * or whose x or gamma overlaps out, is refused with RX_ERR_ARG.  n_norms = 0
+ * is rx_attend_suffix.
  * Errors: those of rx_attend_suffix and rx_adarmsnorm (RX_ERR_ARG for a bad
  * job). */
 rx_status rx_attend_suffix_norms(rx_cache_t cache, int layer, const void* q,
@@ -220,8 +222,10 @@ rx_status rx_attend_suffix_norms(rx_cache_t cache, int layer, const void* q,
                                  int n_norms, void* stream);
 
 /* rx_attend_batch with norm jobs in the same launch, as
- * rx_attend_suffix_norms.  With neither an action suffix nor language
- * streams, the jobs run as rx_adarmsnorm launches. */
+ * rx_attend_suffix_norms (no job may write the action's or the language
+ * streams' inputs, tails or tail lengths, nor read or write their outputs).
+ * With neither an action suffix nor language streams, the jobs run as
+ * rx_adarmsnorm launches. */
 rx_status rx_attend_batch_norms(rx_cache_t cache, int layer, const void* q_act,
                                 const void* k_dyn, const void* v_dyn, int S,
                                 void* out_act, const rx_stream_batch* lang,

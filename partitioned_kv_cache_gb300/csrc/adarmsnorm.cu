@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(kGThreads, 1) ada_gamma_kernel(const __grid_co
   // thread t takes unit kb * 64 + (t % 64) and the vectors k = t / 64 + 4i.
   const int crank = a.cluster > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int csize = a.cluster;
+  // Peers write into this CTA's shared memory below; the matching wait
+  // (before those writes) guarantees every CTA of the cluster has started.
+  if (csize > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int ju = threadIdx.x & 63, kq = threadIdx.x >> 6;
   const __nv_bfloat16* W1s = a.W1 + static_cast<size_t>(set) * a.hidden * cond_dim;
   const __nv_bfloat16* b1s = a.b1 + static_cast<size_t>(set) * a.hidden;
@@ -307,6 +310,7 @@ __global__ void __launch_bounds__(kGThreads, 1) ada_gamma_kernel(const __grid_co
     // after it every CTA holds all of H, and no peer writes into this CTA's
     // shared memory any more.
     __syncthreads();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer has started
     const int n_rows = 2 * a.n_cond;
     const int row = threadIdx.x >> 3;                       // 0..31
     const bool used = threadIdx.x < 8 * 32 && (row < a.n_cond || (row >= 16 && row < 16 + a.n_cond));

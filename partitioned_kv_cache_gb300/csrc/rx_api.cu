@@ -429,6 +429,40 @@ static rx_status check_norms(const char* where, const rx_norm_rows* norms, int n
   return RX_OK;
 }
 
+// A buffer of the attention the norm jobs of the same launch run beside.
+struct Span {
+  const void* p;
+  long long bytes;
+};
+
+static bool spans_overlap(const void* a, long long an, const void* b, long long bn) {
+  if (!a || !b || an <= 0 || bn <= 0) return false;
+  const char* a0 = static_cast<const char*>(a);
+  const char* b0 = static_cast<const char*>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+// The norm jobs run concurrently with the attention of the same launch: no
+// job may write bytes the attention reads or writes, and no job may read
+// bytes the attention writes.
+static rx_status check_norms_beside(const char* where, const rx::NormJob* jobs, int n_norms,
+                                    const Span* att_in, int n_in, const Span* att_out, int n_out) {
+  for (int i = 0; i < n_norms; ++i) {
+    const rx::NormJob& j = jobs[i];
+    if (j.rows == 0) continue;
+    const long long b = static_cast<long long>(j.rows) * j.d * 2;
+    for (int k = 0; k < n_in; ++k)
+      if (spans_overlap(j.y, b, att_in[k].p, att_in[k].bytes))
+        return fail(RX_ERR_ARG, "%s: norm job %d's y overlaps an input of the attention", where, i);
+    for (int k = 0; k < n_out; ++k)
+      if (spans_overlap(j.y, b, att_out[k].p, att_out[k].bytes) ||
+          spans_overlap(j.x, b, att_out[k].p, att_out[k].bytes) ||
+          spans_overlap(j.gamma, static_cast<long long>(j.d) * 4, att_out[k].p, att_out[k].bytes))
+        return fail(RX_ERR_ARG, "%s: norm job %d overlaps the attention's output", where, i);
+  }
+  return RX_OK;
+}
+
 static rx_status attend_suffix_impl(const char* where, rx_cache_t h, int layer, const void* q,
                                     const void* k_dyn, const void* v_dyn, int S, void* out,
                                     const rx_norm_rows* norms, int n_norms, void* stream) {
@@ -441,7 +475,12 @@ static rx_status attend_suffix_impl(const char* where, rx_cache_t h, int layer, 
   if (!aligned16(q) || !aligned16(k_dyn) || !aligned16(v_dyn) || !aligned16(out))
     return fail(RX_ERR_ARG, "%s: pointers must be 16-byte aligned", where);
   rx::NormJob jobs[rx::kMaxNormJobs];
-  const rx_status ns = check_norms(where, norms, n_norms, jobs);
+  rx_status ns = check_norms(where, norms, n_norms, jobs);
+  if (ns != RX_OK) return ns;
+  const long long qb = static_cast<long long>(S) * c.Hq * c.D * 2, kb = static_cast<long long>(S) * c.Hkv * c.D * 2;
+  const Span in[3] = {{q, qb}, {k_dyn, kb}, {v_dyn, kb}};
+  const Span outs[1] = {{out, qb}};
+  ns = check_norms_beside(where, jobs, n_norms, in, 3, outs, 1);
   if (ns != RX_OK) return ns;
   rx::AttnLaunch a = make_launch(h, layer);
   a.norms = jobs;
@@ -653,8 +692,33 @@ static rx_status attend_batch_impl(rx_cache_t h, int layer, const void* q_act, c
                                    b.tail_len, b.T, c.tail_cap, 0};
   }
   rx::NormJob jobs[rx::kMaxNormJobs];
-  const rx_status ns = check_norms("rx_attend_batch", norms, n_norms, jobs);
+  rx_status ns = check_norms("rx_attend_batch", norms, n_norms, jobs);
   if (ns != RX_OK) return ns;
+  {
+    Span in[7] = {};
+    Span outs[2] = {};
+    int n_in = 0, n_out = 0;
+    if (S > 0) {
+      const long long qb = static_cast<long long>(S) * c.Hq * c.D * 2;
+      const long long kb = static_cast<long long>(S) * c.Hkv * c.D * 2;
+      in[n_in++] = {q_act, qb};
+      in[n_in++] = {k_dyn, kb};
+      in[n_in++] = {v_dyn, kb};
+      outs[n_out++] = {out_act, qb};
+    }
+    if (lang && lang->B > 0) {
+      const rx_stream_batch& b = *lang;
+      const long long qb = static_cast<long long>(b.B) * b.T * c.Hq * c.D * 2;
+      const long long tb = static_cast<long long>(b.B) * c.tail_cap * c.Hkv * c.D * 2;
+      in[n_in++] = {b.q, qb};
+      in[n_in++] = {b.k_tail, tb};
+      in[n_in++] = {b.v_tail, tb};
+      in[n_in++] = {b.tail_len, static_cast<long long>(b.B) * 4};
+      outs[n_out++] = {b.out, qb};
+    }
+    ns = check_norms_beside("rx_attend_batch", jobs, n_norms, in, n_in, outs, n_out);
+    if (ns != RX_OK) return ns;
+  }
   int norm_rows = 0;
   for (int i = 0; i < n_norms; ++i) norm_rows += jobs[i].rows;
   if (nseg == 0) {

@@ -147,4 +147,17 @@ def test_norm_job_errors(rx):
     with pytest.raises(rx.RxError) as e:             # negative eps
         cache.attend_suffix(0, q, kd, vd, norms=[(x, g, -1.0, y)])
     assert e.value.status == -1
+    # The norms run beside the attention of the same launch: a norm output on
+    # the attention's q (8 x 2 x 64 = 8 x 128 values), or a norm input under
+    # the attention's output, is refused on both entry points.
+    with pytest.raises(rx.RxError) as e:
+        cache.attend_suffix(0, q, kd, vd, norms=[(x, g, 1e-6, q.view(8, 128))])
+    assert e.value.status == -1
+    with pytest.raises(rx.RxError) as e:
+        cache.attend_suffix(0, q, kd, vd, out=x.view(8, 2, 64), norms=[(x, g, 1e-6, y)])
+    assert e.value.status == -1
+    with pytest.raises(rx.RxError) as e:
+        cache.attend_batch(0, (q, kd, vd), None, norms=[(x, g, 1e-6, q.view(8, 128))])
+    assert e.value.status == -1
+    assert cache.check_device_error() == 0
     cache.close()
