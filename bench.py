@@ -604,6 +604,40 @@ def run_ours(args, wl):
     kern["adarmsnorm_bw_scale"] = {"us": nrm_us, "rows": rows_bw, "bytes": nrm_bytes,
                                    "GB/s": nrm_bytes / nrm_us / 1e3,
                                    "frac_hbm": nrm_bytes / nrm_us / 1e3 / float(peaks["hbm_gbs"])}
+    # The gamma MLP: one launch per tick computes gamma for all 2L sites x K
+    # steps.  Timed alone over weight pools whose W2 together exceed 2x L2, so
+    # each launch streams its weights from DRAM as the tick's does.  Bytes:
+    # the weights (W1, b1, W2, b2, bf16) read once, gamma (fp32) written once.
+    w_bytes = 2.0 * n_sets * (wl.hidden * wl.cond_dim + wl.hidden + wl.d_model * wl.hidden + wl.d_model)
+    g_bytes = 4.0 * n_sets * K * wl.d_model
+    ngp = max(2, int(np.ceil(2 * 129e6 / w_bytes)))
+    gpool = [tuple(randn_bf16(*shp, scale=0.02) for shp in
+                   ((n_sets, wl.hidden, wl.cond_dim), (n_sets, wl.hidden), (n_sets, wl.d_model, wl.hidden),
+                    (n_sets, wl.d_model))) for _ in range(ngp)]
+    gam_out = torch.empty_like(gamma)
+    with torch.cuda.stream(stream):
+        for wp in gpool:
+            rx.ada_gamma(tk, state[0], *wp, wl.emb_dim, out=gam_out)
+    torch.cuda.synchronize()
+    g_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_graph, stream=stream):
+        for wp in gpool:
+            rx.ada_gamma(tk, state[0], *wp, wl.emb_dim, out=gam_out)
+    with torch.cuda.stream(stream):
+        g_graph.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            g_graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    gam_us = e0.elapsed_time(e1) * 1e3 / (3 * ngp)
+    kern["ada_gamma"] = {"us": gam_us, "bytes": w_bytes + g_bytes, "GB/s": (w_bytes + g_bytes) / gam_us / 1e3,
+                         "frac_hbm": (w_bytes + g_bytes) / gam_us / 1e3 / float(peaks["hbm_gbs"]),
+                         "note": "one launch of %d gamma vectors (%d sites x %d steps), graph of %d launches "
+                                 "over distinct weight sets (> 2x L2)" % (n_sets * K, n_sets, K, ngp)}
+    del g_graph, gpool, gam_out
     kern["attention"] = {"us_per_call": plain_us, "flops_per_call": fl, "TFLOP/s": fl / plain_us / 1e6,
                          "frac_tensor": fl / plain_us / 1e6 / peak_tf,
                          "note": "the attention call alone, without the norm jobs"}
