@@ -422,12 +422,14 @@ def test_running_maximum_rescale(rx, splits):
     cache.close()
 
 
-@pytest.mark.parametrize("splits", [1, 0])
+@pytest.mark.parametrize("splits", [1, 0, 18])
 def test_bounded_wait_gives_up_and_reports(rx, splits):
     """A barrier that never completes (the first K tile's barrier of CTA 0
     expects 16 bytes that never arrive): the kernel's waits give up after
     their time limit instead of hanging, the cache's error word reports it
-    (bit 1), and the next call on the same cache matches the oracle."""
+    (bit 1), and the next call on the same cache matches the oracle.  With
+    18 splits (more than a cluster) the timed-out CTA's partial is merged by
+    the combine kernel with l = 0."""
     import time
     wl = W.WORKLOADS["c2"]
     seed = 31
