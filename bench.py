@@ -331,6 +331,119 @@ def attention_call_us(rx, wl, stream, randn_bf16, reps=3):
     return e0.elapsed_time(e1) * 1e3 / (reps * K * L), attn_flops(wl)
 
 
+def graph_us(fn, stream, calls, reps=3):
+    """Per-call time of fn() (`calls` library calls) captured as one CUDA
+    graph after one eager run, replayed `reps` times between CUDA events."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        gr.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+
+def next_rows_kernels(rx, wl, stream, randn_bf16, peaks):
+    """The rows beyond the tick, on the workload's shapes: the block-causal
+    attention call, the push into a ring with a spare slot (the concurrent
+    producer/consumer mode: the frame's tiles are written before the state is
+    published), the language streams' one-token tail append, and a snapshot
+    of the store."""
+    import torch
+    L, S, Hq, Hkv, D, K = wl.L, wl.S, wl.Hq, wl.Hkv, wl.D, wl.steps
+    hbm = float(peaks["hbm_gbs"])
+    out = {}
+    cache = rx.Cache(L, Hq, Hkv, D, wl.P, wl.N, wl.F, S)
+    cache.pin_prefix(randn_bf16(L, wl.P, Hkv, D), randn_bf16(L, wl.P, Hkv, D))
+    with torch.cuda.stream(stream):
+        for _ in range(wl.N):
+            cache.push_frame(randn_bf16(L, wl.F, Hkv, D), randn_bf16(L, wl.F, Hkv, D))
+    q = randn_bf16(K, L, S, Hq, D)
+    kd = randn_bf16(K, L, S, Hkv, D)
+    vd = randn_bf16(K, L, S, Hkv, D)
+    o = torch.empty_like(q)
+
+    def causal():
+        for k in range(K):
+            for l in range(L):
+                cache.attend_suffix(l, q[k, l], kd[k, l], vd[k, l], out=o[k, l], n_state=1)
+
+    us = graph_us(causal, stream, K * L)
+    Lk = wl.P + wl.N * wl.F + S
+    fl = 4.0 * Hq * D * ((S - 1) * Lk + (Lk - (S - 1)))   # the state token's row skips S-1 keys
+    out["attention_block_causal"] = {
+        "us_per_call": us, "flops_per_call": fl, "TFLOP/s": fl / us / 1e6,
+        "frac_tensor": fl / us / 1e6 / float(peaks["bf16_tflops"]),
+        "note": "Eq. 1 with the block-causal mask (the state token sees only its own dynamic key, the "
+                "%d action tokens every key); %d calls per graph" % (S - 1, K * L)}
+    nb = cache.snapshot_bytes()
+    snap = torch.empty(nb, dtype=torch.uint8, device=q.device)
+    with torch.cuda.stream(stream):
+        cache.snapshot(snap)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            cache.snapshot(snap)
+        e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 5
+    out["snapshot"] = {"us": us, "bytes": 2.0 * nb, "GB/s": 2.0 * nb / us / 1e3,
+                       "frac_hbm": 2.0 * nb / us / 1e3 / hbm,
+                       "note": "device copy of the store's regions and ring state (%.1f MB read + written)"
+                               % (nb / 1e6)}
+    assert cache.check_device_error() == 0, "a kernel reported a device-side timeout"
+    cache.close()
+    del q, kd, vd, o, snap
+
+    sp = rx.Cache(L, Hq, Hkv, D, wl.P, wl.N, wl.F, S, spare_slot=1)
+    fb = 2 * L * wl.F * Hkv * D * 2
+    nfr = max(2, int(np.ceil(2 * 129e6 / fb)))
+    pool = [(randn_bf16(L, wl.F, Hkv, D), randn_bf16(L, wl.F, Hkv, D)) for _ in range(nfr)]
+
+    def pushes():
+        for fr in pool:
+            sp.push_frame(*fr)
+
+    us = graph_us(pushes, stream, nfr)
+    out["ring_append_spare_slot"] = {
+        "us": us, "bytes": 2.0 * fb, "GB/s": 2.0 * fb / us / 1e3, "frac_hbm": 2.0 * fb / us / 1e3 / hbm,
+        "note": "one push of all %d layers into a ring with a spare slot, graph of %d pushes over distinct "
+                "frames (> 2x L2)" % (L, nfr)}
+    assert sp.check_device_error() == 0, "a kernel reported a device-side timeout"
+    sp.close()
+    del pool
+
+    B, cap = max(wl.n_lang, 16), max(wl.tail_cap, 32)
+    tk = randn_bf16(L, B, cap, Hkv, D)
+    tv = randn_bf16(L, B, cap, Hkv, D)
+    tl = torch.zeros((L, B), dtype=torch.int32, device=tk.device)
+    nk = randn_bf16(L, B, Hkv, D)
+    nv = randn_bf16(L, B, Hkv, D)
+
+    def appends():
+        tl.zero_()
+        for l in range(L):
+            rx.tail_append(tk[l], tv[l], tl[l], nk[l], nv[l])
+
+    us = graph_us(appends, stream, L)
+    tb = 2.0 * 2 * B * Hkv * D * 2
+    out["tail_append"] = {"us": us, "bytes": tb, "GB/s": tb / us / 1e3,
+                          "note": "one token appended to each of %d language streams' tails (one call per "
+                                  "layer, %d calls per graph): latency-bound" % (B, L)}
+    return out
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -638,6 +751,7 @@ def run_ours(args, wl):
                          "note": "one launch of %d gamma vectors (%d sites x %d steps), graph of %d launches "
                                  "over distinct weight sets (> 2x L2)" % (n_sets * K, n_sets, K, ngp)}
     del g_graph, gpool, gam_out
+    kern.update(next_rows_kernels(rx, wl, stream, randn_bf16, peaks))
     kern["attention"] = {"us_per_call": plain_us, "flops_per_call": fl, "TFLOP/s": fl / plain_us / 1e6,
                          "frac_tensor": fl / plain_us / 1e6 / peak_tf,
                          "note": "the attention call alone, without the norm jobs"}
