@@ -921,12 +921,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // lane loads up to 16 of its splits at a time, so up to 32 splits are in
 // flight per (row, piece).  More splits run with a running maximum.  The
 // pair's (M, L, sums) meet by one shuffle.  Compiled with a register cap
-// (128) rather than a thread bound: the same 128 registers, and c4's call
-// 11.93 -> 11.76 us in an A/B on one GB300.
+// rather than a thread bound: 128 registers either way, but c4's call took
+// 11.93 us with the bound, 11.76 us with a cap of 128 and 11.61 us with 132
+// or 136 (A/Bs on one GB300).  A cap that lets it use more (140 and up)
+// keeps a second combine CTA off each SM and was slower (12.0 us).
 constexpr int kCombineChunk = 16;
 
 template <int D>
-__global__ void __maxnreg__(128) attn_combine_kernel(const uint4* __restrict__ xchg,
+__global__ void __maxnreg__(136) attn_combine_kernel(const uint4* __restrict__ xchg,
                                                            __nv_bfloat16* out0, int rows0, int m_tiles0,
                                                            __nv_bfloat16* out1, int rows1, int n_splits,
                                                            int dparts, int Hq, int G) {
