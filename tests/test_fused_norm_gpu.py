@@ -124,6 +124,15 @@ def test_batch_with_norm_jobs(rx):
     jobs2, host2 = _jobs(seed + 7, [(20, 1024)])
     cache.attend_batch(0, None, None, norms=jobs2)
     _check_jobs(rx, jobs2, host2)
+    # The language streams alone (their segment is the launch's only one)
+    # with the layer's two norms.
+    jobs3, host3 = _jobs(seed + 9, [(51, 1024), (51, 1024)])
+    _, ol3 = cache.attend_batch(1, None, lang, norms=jobs3)
+    _, pl3 = cache.attend_batch(1, None, lang)
+    assert torch.equal(ol3, pl3)
+    for b, ref in enumerate(OA.shared_cache_attention(ks[:-1], vs[:-1], reqs)):
+        check_attention(host64(ol3[b]), ref)
+    _check_jobs(rx, jobs3, host3)
     assert cache.check_device_error() == 0
     cache.close()
 
