@@ -918,14 +918,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // pieces (its 8 warps, one piece each), so the rows' (m, l) are fetched from
 // L2 once per CTA and served to the other warps from L1.  Grid: (M-tiles of
 // all segments x 8 row groups, pieces / 8, Hkv x dparts), 256 threads.  Each
-// lane loads up to 16 of its splits at a time, so up to 32 splits are in
-// flight per (row, piece).  More splits run with a running maximum.  The
+// lane loads up to kCombineChunk of its splits at a time, so up to 28 splits
+// are in flight per (row, piece).  More splits run with a running maximum.  The
 // pair's (M, L, sums) meet by one shuffle.  Compiled with a register cap
 // rather than a thread bound: 128 registers either way, but c4's call took
 // 11.93 us with the bound, 11.76 us with a cap of 128 and 11.61 us with 132
 // or 136 (A/Bs on one GB300).  A cap that lets it use more (140 and up)
-// keeps a second combine CTA off each SM and was slower (12.0 us).
-constexpr int kCombineChunk = 16;
+// keeps a second combine CTA off each SM and was slower (12.0 us).  A lane
+// loads up to 14 splits at a time: the 27 splits of c4's partition in one
+// pass (11.75 -> 11.61 us per call against 16 at a time).
+constexpr int kCombineChunk = 14;
 
 template <int D>
 __global__ void __maxnreg__(136) attn_combine_kernel(const uint4* __restrict__ xchg,
