@@ -92,7 +92,7 @@ typedef struct rx_config {
 rx_status rx_cache_create(const rx_config* cfg, rx_cache_t* out);
 
 /* Free everything the cache owns.  Synchronises the device first.  NULL is a
- * no-op. */
+ * no-op.  Errors: RX_ERR_CUDA (the synchronisation or the free failed). */
 rx_status rx_cache_destroy(rx_cache_t cache);
 
 /* Copy the instruction prefix into the pinned region ("Reflex ...", §III
@@ -225,7 +225,8 @@ rx_status rx_attend_suffix_norms(rx_cache_t cache, int layer, const void* q,
  * rx_attend_suffix_norms (no job may write the action's or the language
  * streams' inputs, tails or tail lengths, nor read or write their outputs).
  * With neither an action suffix nor language streams, the jobs run as
- * rx_adarmsnorm launches. */
+ * rx_adarmsnorm launches.  Errors: those of rx_attend_batch and
+ * rx_adarmsnorm (RX_ERR_ARG for a bad or overlapping job). */
 rx_status rx_attend_batch_norms(rx_cache_t cache, int layer, const void* q_act,
                                 const void* k_dyn, const void* v_dyn, int S,
                                 void* out_act, const rx_stream_batch* lang,
@@ -297,19 +298,22 @@ rx_status rx_adarmsnorm(const void* x, const float* gamma, int rows, int d,
 
 /* Read the device-side ring state (synchronises `stream`): head = slot the
  * next push writes, valid = frames held, pushes = pushes applied on the
- * device (advances under CUDA-graph replay too).  Any pointer may be NULL. */
+ * device (advances under CUDA-graph replay too).  Any pointer may be NULL.
+ * Errors: RX_ERR_ARG (null cache), RX_ERR_CUDA. */
 rx_status rx_get_state(rx_cache_t cache, int* head, int* valid,
                        long long* pushes, void* stream);
 
 /* Test aid: the window's physical slots in logical order, oldest first
  * (slots: host int[N], the first *valid entries are filled).  Reads the
- * device state (synchronises `stream`). */
+ * device state (synchronises `stream`).  Errors: RX_ERR_ARG (null argument),
+ * RX_ERR_CUDA. */
 rx_status rx_debug_window(rx_cache_t cache, int* slots, int* valid,
                           void* stream);
 
 /* Test aid: copy one layer's window in logical order (oldest frame first)
  * into k_out, v_out: device bf16 [valid*F][Hkv][D].  Reads the device state
- * (synchronises `stream`), then enqueues the copies. */
+ * (synchronises `stream`), then enqueues the copies.  Errors: RX_ERR_ARG
+ * (null argument), RX_ERR_LAYER, RX_ERR_UNSUPPORTED (N > 4096), RX_ERR_CUDA. */
 rx_status rx_export_window(rx_cache_t cache, int layer, void* k_out,
                            void* v_out, void* stream);
 
@@ -350,7 +354,8 @@ rx_status rx_debug_choose_partition(int t_max, int units, int D, int num_sms, in
 
 /* Number of split-KV partitions for attention launches of this cache
  * (0 = chosen from the SM count, the default).  A tuning knob: results are
- * the same for every value up to rounding order. */
+ * the same for every value up to rounding order.  Errors: RX_ERR_ARG (null
+ * cache, or splits outside [0, the workspace's capacity]). */
 rx_status rx_set_attn_splits(rx_cache_t cache, int splits);
 
 /* Number of CTAs that share the output columns of one (query tile, split):
@@ -361,7 +366,7 @@ rx_status rx_set_attn_splits(rx_cache_t cache, int splits);
 rx_status rx_set_attn_dparts(rx_cache_t cache, int dparts);
 
 /* Kernel launches made by the library in this process (all entry points,
- * all caches).  For accounting in benchmarks. */
+ * all caches).  For accounting in benchmarks.  Cannot fail. */
 long long rx_launch_count(void);
 
 const char* rx_status_str(int status);
