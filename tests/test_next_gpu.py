@@ -47,6 +47,28 @@ def test_block_causal_suffix(rx, name, n_state):
     cache.close()
 
 
+@pytest.mark.parametrize("name", ["c3", "c4"])
+def test_block_causal_suffix_at_full_size(rx, name):
+    """The full-size stores with one state token, as the benchmark times the
+    masked call: every row of the first and last layer after a full window
+    (c4: 27 key splits merged by the combine kernel, the mask in the last
+    split's dynamic tile).  c4's ×20 outlier keys make the output scale
+    max|ref|, and both bounds are taken relative to it."""
+    wl = W.WORKLOADS[name]
+    seed = 43
+    cache, ost = _stream_cache(rx, wl, seed, wl.N + 1)
+    f = W.bf16_bits_to_f64
+    for layer in (0, wl.L - 1):
+        q, kd, vd = W.suffix_qkv(wl, seed, wl.N, 3, layer)
+        got = host64(cache.attend_suffix(layer, dev(q), dev(kd), dev(vd), n_state=1))
+        ks, vs = ost.regions(layer, f(kd), f(vd))
+        ref = OA.block_causal_attention(f(q), ks, vs, 1)
+        scale = max(1.0, float(np.abs(ref).max())) if wl.outlier_frac > 0 else 1.0
+        check_attention(got, ref, scale)
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
 def test_tail_append_follows_the_host_model_and_reports_overflow(rx):
     import torch
     B, cap, Hkv, D = 5, 4, 1, 64

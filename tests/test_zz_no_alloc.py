@@ -21,12 +21,15 @@ from tests._util import check_attention, dev, ensure_built, few_keys_scale, host
 pytestmark = pytest.mark.gpu
 
 # (S, Hq, Hkv, D, P, W, n_dyn): the single-layer benchmark shape (whose
-# 408 query rows leave room for 30 of the 64 splits in the scratch), empty
+# 408 query rows leave room for 30 of the 64 splits in the scratch), the
+# long-history store's 8448 cached keys (27 key splits merged by the combine
+# kernel, their partials in the fixed scratch), empty
 # regions, a window that is not a multiple of 64 tokens, G of 1 and 2,
 # D of 64 and 128, and a 1024-token suffix whose 8192 rows leave room for one
 # split only.
 CASES = [
     (51, 8, 1, 256, 48, 1024, 51),
+    (51, 8, 1, 256, 256, 8192, 51),
     (51, 8, 1, 256, 0, 1024, 51),
     (51, 8, 1, 256, 48, 0, 51),
     (51, 8, 1, 256, 48, 1024, 0),
