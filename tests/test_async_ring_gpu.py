@@ -52,6 +52,35 @@ def test_spare_slot_ring_on_one_stream(rx):
     cache.close()
 
 
+def test_spare_slot_ring_at_the_long_history_size(rx):
+    """c4's window of 32 frames with a spare slot (33 physical slots, two
+    layers): once the ring is full, the slot a push is about to overwrite is
+    left out of the window, and with each push that gap moves to another of
+    the 27 key splits.  Every checked call must see exactly the last N
+    frames.  The ×20 outlier keys make the output scale max|ref|, and both
+    bounds are taken relative to it."""
+    import dataclasses
+    wl = dataclasses.replace(W.WORKLOADS["c4"], L=2)
+    seed = 54
+    cache = _cache(rx, wl, seed)
+    ost = OracleStream(wl, seed)
+    f = W.bf16_bits_to_f64
+    check_at = {wl.N - 1, wl.N, wl.N + 1, wl.N + 9, wl.N + 17, wl.N + 26, 2 * wl.N + 1}
+    for t in range(2 * wl.N + 2):
+        fk, fv = W.frame_kv(wl, seed, t)
+        assert cache.push_frame(dev(fk), dev(fv)) == ost.push(t)
+        if t not in check_at:
+            continue
+        q, kd, vd = W.suffix_qkv(wl, seed, t, 0, 1)
+        got = host64(cache.attend_suffix(1, dev(q), dev(kd), dev(vd)))
+        ks, vs = ost.regions(1, f(kd), f(vd))
+        ref = OA.partitioned_attention(f(q), ks, vs)
+        scale = max(1.0, float(np.abs(ref).max())) if wl.outlier_frac > 0 else 1.0
+        check_attention(got, ref, scale)
+    assert cache.check_device_error() == 0
+    cache.close()
+
+
 def test_concurrent_pushes_never_tear_the_window(rx):
     import torch
     wl = W.WORKLOADS["c2"]
