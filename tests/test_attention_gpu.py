@@ -380,8 +380,11 @@ def test_running_maximum_rescale(rx, splits):
     keys carry ~15% of the weight with values near +1 and the jumping key's
     value is -1, so a wrong rescale factor moves the output visibly.  One split
     walks every tile in order.  The output is of order 1, so the bound is the
-    rounding of the path, not the unit-scale tolerance: bf16 output rounding
-    (2^-9 |o|) plus bf16 P in the P V product (2^-9 max|v|), doubled."""
+    rounding of the path, not the unit-scale tolerance.  bf16 keeps 8
+    significant bits (a rounding to nearest is within 2^-8 of the value): the
+    output rounding (2^-8 |o|) plus bf16 P in the P V product (2^-8 max|v|).
+    With two splits each split's partial is rounded to bf16 too, and the case
+    is still held to that two-rounding bound."""
     D, G, S, P, N, F = 64, 8, 51, 64, 4, 64
     rng = np.random.default_rng(77)
     u = np.zeros(D, np.float32)
