@@ -82,8 +82,10 @@ def test_zero_rows_is_a_noop(rx):
 ])
 def test_gamma_shapes_and_scales(rx, d, hidden, emb, state_dim, n_cond, wscale):
     """Eq. (2)'s gamma MLP over the edge shapes of the kernel.  Bound: the
-    error of an fp32 evaluation with the hidden activation carried to ~2^-17
-    (two bf16 parts), 4e-5 x sum_j |W2_ij h_j| + |b2_i| per element."""
+    error of an fp32 evaluation with the hidden activation carried to 2^-16
+    of itself (two bf16 parts: the second holds the first's rounding error,
+    itself rounded within 2^-8), 4e-5 x sum_j |W2_ij h_j| + |b2_i| per
+    element."""
     import torch
     wl = W.Workload("gamma-shape", L=1, Hq=1, Hkv=1, D=64, P=0, N=1, F=1, S=1, steps=n_cond,
                     ticks=1, d_model=d, emb_dim=emb, state_dim=state_dim, hidden=hidden)
