@@ -49,6 +49,9 @@ def test_forced_values_are_kept_and_clamped(rx):
     assert choose(rx, 18, 4, splits=20, dparts=1) == (18, 1, False)   # clamped to the key tiles
     assert choose(rx, 133, 4, splits=24, dparts=1) == (24, 1, False)  # beyond a cluster: combine kernel
     assert choose(rx, 133, 4, max_splits=8) == (8, 2, True)     # the workspace holds 8 splits
+    # The allocation-free entry point's 8 MiB scratch holds 30 splits of c4's
+    # 408 query rows: the same 27 as the cache's workspace.
+    assert choose(rx, 133, 4, max_splits=30) == (27, 1, False)
 
 
 def test_out_of_range_sizes_are_refused(rx):
